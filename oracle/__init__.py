@@ -68,7 +68,7 @@ def _load():
         lib.oracle_e4m3_decode_array.restype = None
         lib.oracle_e4m3_decode_array.argtypes = [P, i64, P]
         lib.oracle_store_kv.restype = i32
-        lib.oracle_store_kv.argtypes = [P, P, P, i64, i64, i64, P, P, P, P, P, P, i64]
+        lib.oracle_store_kv.argtypes = [P, P, P, i64, i64, i64, i64, P, P, P, P, P, P, i64]
         lib.oracle_decode.restype = i32
         lib.oracle_decode.argtypes = [P, P, P, i32, P, P, i64, i32, i32, i32, P, i32, P, i32, i32,
                                       dbl, P, i32]
@@ -116,10 +116,12 @@ def store_kv(k, v, slot_mapping, k_cache, v_cache, k_scale_new=None, v_scale_new
     k, v: (T, Hkv, D) uint16 (bf16 bits) or uint8 (E4M3); caches:
     (num_blocks, block_size, Hkv, D) of the same dtype, modified in place;
     slot_mapping (T,) int64, slot = block * block_size + offset, < 0 skips.
+    FP8 scales: new (T, Hkv) fp32 -> caches (num_blocks, Hkv, block_size).
     """
     T = k.shape[0]
     row_bytes = k[0].nbytes if T else k_cache[0, 0].nbytes
     num_slots = k_cache.shape[0] * k_cache.shape[1]
+    block_size = k_cache.shape[1]
     hkv = k_cache.shape[2]
     for a in (k_cache, v_cache, k_scale_cache, v_scale_cache):
         if a is not None and not a.flags.c_contiguous:
@@ -129,7 +131,7 @@ def store_kv(k, v, slot_mapping, k_cache, v_cache, k_scale_new=None, v_scale_new
     ks = None if k_scale_new is None else _c(k_scale_new, np.float32)
     vs = None if v_scale_new is None else _c(v_scale_new, np.float32)
     _check(_load().oracle_store_kv(_ptr(k), _ptr(v), _ptr(sm), T, row_bytes, num_slots,
-                                   _ptr(k_cache), _ptr(v_cache), _ptr(ks), _ptr(vs),
+                                   block_size, _ptr(k_cache), _ptr(v_cache), _ptr(ks), _ptr(vs),
                                    _ptr(k_scale_cache), _ptr(v_scale_cache), hkv))
 
 

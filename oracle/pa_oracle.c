@@ -34,7 +34,8 @@
  * notes): slot = physical_block * block_size + offset, negative slot = skip;
  * cache layout (num_blocks, block_size, num_kv_heads, head_dim) row-major for
  * both K and V; FP8 is OCP E4M3 with one fp32 scale per (slot, kv head) in a
- * (num_blocks, block_size, num_kv_heads) array; context_len 0 gives a zero
+ * (num_blocks, num_kv_heads, block_size) array (one head's scales for one
+ * block are contiguous); context_len 0 gives a zero
  * output row; a prefill sequence with q_len > kv_len is invalid input.
  */
 #include <math.h>
@@ -80,27 +81,32 @@ void oracle_e4m3_decode_array(const uint8_t* codes, int64_t n, double* out) {
 
 /* ------------------------------------------------------------------------ */
 /* store_kvcache: write each new token's K and V rows into its cache slot.
- * [TVL] scatter section: block = slot / block_size, offset = slot % block_size
- * (here the slot already encodes both). Bytes are copied verbatim.
+ * [TVL] scatter section: block = slot / block_size, offset = slot % block_size.
+ * Bytes are copied verbatim.
  * k, v: (T, row_bytes); caches: (num_slots, row_bytes) where
  * num_slots = num_blocks * block_size and row_bytes = Hkv * D * elem_size.
- * Optional FP8 scale rows (T, Hkv) -> (num_slots, Hkv) are copied likewise. */
+ * Optional FP8 scales (T, Hkv) go to scale caches (num_blocks, Hkv, block_size):
+ * head h of the token lands at [block][h][offset]. */
 int oracle_store_kv(const uint8_t* k, const uint8_t* v, const int64_t* slot_mapping,
-                    int64_t T, int64_t row_bytes, int64_t num_slots,
+                    int64_t T, int64_t row_bytes, int64_t num_slots, int64_t block_size,
                     uint8_t* k_cache, uint8_t* v_cache,
                     const float* k_scale_new, const float* v_scale_new,
                     float* k_scale_cache, float* v_scale_cache, int64_t hkv) {
-  if (!k || !v || !slot_mapping || !k_cache || !v_cache || row_bytes <= 0) return OR_ERR_ARG;
+  if (!k || !v || !slot_mapping || !k_cache || !v_cache || row_bytes <= 0 || block_size <= 0)
+    return OR_ERR_ARG;
   for (int64_t t = 0; t < T; ++t) {
     int64_t slot = slot_mapping[t];
     if (slot < 0) continue; /* padding token: nothing is written */
     if (slot >= num_slots) return OR_ERR_RANGE;
+    int64_t block = slot / block_size, offset = slot % block_size;
     memcpy(k_cache + slot * row_bytes, k + t * row_bytes, (size_t)row_bytes);
     memcpy(v_cache + slot * row_bytes, v + t * row_bytes, (size_t)row_bytes);
-    if (k_scale_new && k_scale_cache)
-      memcpy(k_scale_cache + slot * hkv, k_scale_new + t * hkv, (size_t)hkv * sizeof(float));
-    if (v_scale_new && v_scale_cache)
-      memcpy(v_scale_cache + slot * hkv, v_scale_new + t * hkv, (size_t)hkv * sizeof(float));
+    for (int64_t h = 0; h < hkv; ++h) {
+      if (k_scale_new && k_scale_cache)
+        k_scale_cache[(block * hkv + h) * block_size + offset] = k_scale_new[t * hkv + h];
+      if (v_scale_new && v_scale_cache)
+        v_scale_cache[(block * hkv + h) * block_size + offset] = v_scale_new[t * hkv + h];
+    }
   }
   return OR_OK;
 }
@@ -117,12 +123,14 @@ typedef struct {
 } or_cache;
 
 /* Element (slot, kv head, dim) of a cache, widened to double (times the
- * per-(slot, head) scale for E4M3). */
+ * per-(slot, head) scale for E4M3, stored at [block][head][offset]). */
 static double cache_elem(const or_cache* c, const void* base, const float* scale,
                          int64_t slot, int g, int dim) {
   int64_t idx = (slot * c->hkv + g) * c->d + dim;
   if (c->dtype == OR_KV_BF16) return bf16_to_double(((const uint16_t*)base)[idx]);
-  return oracle_e4m3_to_double(((const uint8_t*)base)[idx]) * (double)scale[slot * c->hkv + g];
+  int64_t block = slot / c->block_size, offset = slot % c->block_size;
+  double sc = (double)scale[(block * c->hkv + g) * c->block_size + offset];
+  return oracle_e4m3_to_double(((const uint8_t*)base)[idx]) * sc;
 }
 
 /* Slot of logical position p of sequence b, through the block table

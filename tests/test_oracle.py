@@ -273,10 +273,11 @@ def test_fp8_decode_equals_dense_attention_on_dequantised_values():
                     inp.k_scale_new.numpy(), inp.v_scale_new.numpy(), ksc, vsc)
     got = oracle.decode(_bits(inp.q), kc, vc, inp.block_tables.numpy(), inp.context_lens.numpy(),
                         inp.scale, k_scale=ksc, v_scale=vsc)
+    # scales are stored (NB, Hkv, bs); bring them to the cache's (NB, bs, Hkv)
     kd = torch.from_numpy(kc).view(torch.float8_e4m3fn).to(torch.float64) * \
-        torch.from_numpy(ksc).double()[..., None]
+        torch.from_numpy(ksc).double().permute(0, 2, 1)[..., None]
     vd = torch.from_numpy(vc).view(torch.float8_e4m3fn).to(torch.float64) * \
-        torch.from_numpy(vsc).double()[..., None]
+        torch.from_numpy(vsc).double().permute(0, 2, 1)[..., None]
     dense = W.DecodeInputs(**{**inp.__dict__, "k_cache": kd, "v_cache": vd})
     G = H // Hkv
     for b, L in enumerate(lens):

@@ -6,8 +6,8 @@ library's tests/bench and the CPU oracle can consume what it produces.
 
 Layouts (the library's boundary):
   * k_cache, v_cache: (num_blocks, block_size, num_kv_heads, head_dim),
-    bf16 or FP8-E4M3 (stored as uint8 codes); FP8 adds fp32 scales
-    (num_blocks, block_size, num_kv_heads).
+    bf16 or FP8-E4M3 (stored as uint8 codes); FP8 adds fp32 scales, one per
+    (slot, kv head), laid out (num_blocks, num_kv_heads, block_size).
   * block_tables: (batch, max_blocks) int32, unused entries -1.
   * slot = physical_block * block_size + offset (int64), one per new token.
 
@@ -70,7 +70,7 @@ class DecodeInputs:
     context_lens: torch.Tensor      # (B,) int32, includes the new token
     scale: float
     kv_dtype: str = "bf16"
-    k_scale: torch.Tensor | None = None       # (NB, bs, Hkv) fp32 (FP8 only)
+    k_scale: torch.Tensor | None = None       # (NB, Hkv, bs) fp32 (FP8 only)
     v_scale: torch.Tensor | None = None
     k_scale_new: torch.Tensor | None = None   # (B, Hkv) fp32 (FP8 only)
     v_scale_new: torch.Tensor | None = None
@@ -200,6 +200,8 @@ def make_decode(batch: int, num_heads: int, num_kv_heads: int, head_dim: int, bl
     elif kv_dtype == "fp8":
         k_cache, ks = _randn_fp8(cache_shape, g, device)
         v_cache, vs = _randn_fp8(cache_shape, g, device)
+        ks = ks.permute(0, 2, 1).contiguous()  # (NB, Hkv, bs)
+        vs = vs.permute(0, 2, 1).contiguous()
         k_new, ksn = _randn_fp8((batch, num_kv_heads, head_dim), g, device)
         v_new, vsn = _randn_fp8((batch, num_kv_heads, head_dim), g, device)
     else:
