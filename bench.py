@@ -1,0 +1,453 @@
+"""Benchmark of the paged decode hot path on GB300.
+
+One step = pa_store_kv of the batch's new tokens + pa_decode over the whole
+batch (split kernel and, when a sequence needs several splits, the merge
+kernel), on the Llama-3-8B-shaped workload (batch 64, 32/8 heads, head_dim 128,
+block_size 16, context_len ~ U[512, 4096]) unless --workload says otherwise.
+
+Prints ONE JSON line (rank 0). Inputs are resident in HBM before timing; the
+step rotates over several independently drawn KV pools so consecutive steps
+never re-read KV from L2. The dominant launch (pa_decode) is also timed on its
+own with CUDA events inside the timed region for the roofline figure.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the CPU oracle as the reference arm
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import workloads as W  # noqa: E402
+
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+L2_BYTES = 129 * 2 ** 20
+METRIC = "Paged decode attention KV-cache GB/s (% of GB300 HBM peak), seq-steps/s"
+DEFAULT_WORKLOAD = "llama3_8b_decode_b64"
+
+
+def kv_bytes(name: str, lens) -> int:
+    w = W.WORKLOADS[name]
+    eb = 1 if w["kv_dtype"] == "fp8" else 2
+    per_tok = w["num_kv_heads"] * w["head_dim"] * eb * 2
+    if w["kv_dtype"] == "fp8":
+        per_tok += w["num_kv_heads"] * 4 * 2  # one fp32 scale per (token, head) for K and V
+    return int(sum(lens)) * per_tok
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        hbm = d.get("hbm_gbs") or d.get("hbm_GBps") or d.get("hbm")
+        if isinstance(hbm, dict):
+            hbm = hbm.get("value")
+        if hbm:
+            return float(hbm), "measured"
+    except (OSError, ValueError):
+        pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def traffic_from_profile(kernel_file: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel source (the summary records the source's sha256)."""
+    src = os.path.join(ROOT, "paged_kv_cache_186_gb300", "csrc", kernel_file)
+    prof = os.path.join(ROOT, "profiles", f"decode_split_kernel_{workload}.md")
+    try:
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        text = open(prof).read()
+    except OSError:
+        return None
+    m_sha = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
+    m_tr = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    if not m_sha or not m_tr or m_sha.group(1) != sha:
+        return None
+    return float(m_tr.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples while the timed region runs."""
+    Q = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.lines = []
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-i", str(gpu_index), "-lms", "100"], stdout=subprocess.PIPE,
+                stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self, t0: float, t1: float):
+        rows = []
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                rows.append((ts, float(parts[2]), float(parts[3]), parts[5:]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        inside = [r for r in rows if t0 - 1.0 <= r[0] <= t1 + 1.0] or rows
+        sm = sorted(r[1] for r in inside)
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for r in inside:
+            for name, v in zip(names, r[3][1:]):
+                if v.strip().lower() in ("active", "0x1", "1"):
+                    reasons.add(name)
+        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": max(r[2] for r in inside),
+                "reasons": sorted(reasons), "samples": len(inside)}
+
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if (args.impl == "gpu" and torch.cuda.is_available()) else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    elif args.impl == "gpu":
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(world, x: float) -> float:
+    if world <= 1:
+        return x
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(world, x: float) -> float:
+    if world <= 1:
+        return x
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ CPU oracle
+def oracle_sample(name: str, max_seqs: int, seed: int = 0):
+    """Host inputs for a bounded sample of a decode workload: the first
+    `max_seqs` of its sequences (same lengths, shapes and value recipe, a pool
+    just big enough for them)."""
+    w = W.WORKLOADS[name]
+    lens = W.workload_lengths(name)[:max_seqs]
+    kw = {}
+    if w.get("sinks"):
+        kw["sinks"] = w["sinks"]
+    h = W.make_decode(len(lens), w["num_heads"], w["num_kv_heads"], w["head_dim"],
+                      w["block_size"], lens, seed=w["seed"] + 7 + seed, kv_dtype=w["kv_dtype"],
+                      scale=w["scale"], **kw)
+    return h, lens
+
+
+def run_oracle_step(h, threads: int):
+    import oracle
+    if h.kv_dtype == "bf16":
+        kc, vc = W.bf16_bits(h.k_cache).copy(), W.bf16_bits(h.v_cache).copy()
+        t0 = time.perf_counter()
+        oracle.store_kv(W.bf16_bits(h.k_new), W.bf16_bits(h.v_new), h.slot_mapping.numpy(), kc, vc)
+        oracle.decode(W.bf16_bits(h.q), kc, vc, h.block_tables.numpy(), h.context_lens.numpy(),
+                      h.scale, threads=threads)
+        return time.perf_counter() - t0
+    kc, vc = W.u8(h.k_cache).copy(), W.u8(h.v_cache).copy()
+    ks, vs = h.k_scale.numpy().copy(), h.v_scale.numpy().copy()
+    t0 = time.perf_counter()
+    oracle.store_kv(W.u8(h.k_new), W.u8(h.v_new), h.slot_mapping.numpy(), kc, vc,
+                    h.k_scale_new.numpy(), h.v_scale_new.numpy(), ks, vs)
+    oracle.decode(W.bf16_bits(h.q), kc, vc, h.block_tables.numpy(), h.context_lens.numpy(),
+                  h.scale, k_scale=ks, v_scale=vs, threads=threads)
+    return time.perf_counter() - t0
+
+
+def sample_size_for(name: str, budget_s: float, threads: int) -> int:
+    """Sequences per oracle step so one step takes about budget_s (estimated
+    from a 1-sequence probe)."""
+    h, lens = oracle_sample(name, 1)
+    dt = max(run_oracle_step(h, threads), 1e-4)
+    per_tok = dt / max(1, sum(lens))
+    all_lens = W.workload_lengths(name)
+    n, acc = 0, 0.0
+    for L in all_lens:
+        if n > 0 and acc + L * per_tok > budget_s:
+            break
+        acc += L * per_tok
+        n += 1
+    return max(1, n)
+
+
+def cpu_baseline(name: str, budget_s: float = 15.0):
+    import oracle
+    oracle.build()
+    threads = len(os.sched_getaffinity(0))
+    n = sample_size_for(name, budget_s, threads)
+    h, lens = oracle_sample(name, n)
+    dt = run_oracle_step(h, threads)
+    return {"value": kv_bytes(name, lens) / dt / 1e9, "unit": "GB/s", "cores": threads,
+            "kind": "oracle",
+            "sample": f"first {n} of {len(W.workload_lengths(name))} sequences "
+                      f"({sum(lens)} keys), one store_kv+decode, fp64 C oracle, {dt:.2f} s"}
+
+
+def run_reference(args, world, rank):
+    name = args.workload
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    threads = len(os.sched_getaffinity(0))
+    budget = max(0.5, 120.0 / max(1, args.steps + args.warmup))
+    n = sample_size_for(name, budget, threads)
+    h, lens = oracle_sample(name, n)
+    for _ in range(args.warmup):
+        run_oracle_step(h, threads)
+    t = 0.0
+    for _ in range(args.steps):
+        t += run_oracle_step(h, threads)
+    per_step = t / max(1, args.steps)
+    bytes_step = kv_bytes(name, lens)
+    value = bytes_step / per_step / 1e9
+    w = W.WORKLOADS[name]
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_step * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic",
+        "config": {"workload": name, "batch": n, "num_heads": w["num_heads"],
+                   "num_kv_heads": w["num_kv_heads"], "head_dim": w["head_dim"],
+                   "block_size": w["block_size"], "kv_dtype": w["kv_dtype"],
+                   "sample_of_batch": f"{n}/{w['batch']}"},
+        "seq_steps_per_s": n / per_step,
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                         "sample": f"first {n} of {w['batch']} sequences per step"},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ GPU arm
+def run_gpu(args, world, rank, local):
+    import paged_kv_cache_186_gb300 as pa
+    from paged_kv_cache_186_gb300 import build as pabuild
+    if rank == 0 or world == 1:
+        pabuild.build()
+    barrier(world)
+    name = args.workload
+    w = W.WORKLOADS[name]
+    dev = torch.device("cuda", torch.cuda.current_device())
+    lens = W.workload_lengths(name)
+    B = w["batch"]
+    step_bytes = kv_bytes(name, lens)
+    pool_bytes = step_bytes
+    n_pools = max(2, min(4, math.ceil(4 * L2_BYTES / max(1, pool_bytes)) + 1))
+    pools = [W.make_workload(name, device=dev, variant=v + 97 * rank) for v in range(n_pools)]
+    fp8 = w["kv_dtype"] == "fp8"
+    max_len = max(lens)
+    ws_bytes = pa.decode_workspace_size(pools[0].k_cache, B, w["num_heads"],
+                                        pools[0].block_tables.shape[1], max_len,
+                                        k_scale=pools[0].k_scale, v_scale=pools[0].v_scale)
+    workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+    out = torch.empty((B, w["num_heads"], w["head_dim"]), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(p, ev=None):
+        pa.store_kv(p.k_new, p.v_new, p.slot_mapping, p.k_cache, p.v_cache, p.k_scale_new,
+                    p.v_scale_new, p.k_scale, p.v_scale)
+        if ev is not None:
+            ev[0].record(stream)
+        pa.decode(p.q, p.k_cache, p.v_cache, p.block_tables, p.context_lens, p.scale,
+                  max_context_len=max_len, out=out, workspace=workspace, k_scale=p.k_scale,
+                  v_scale=p.v_scale)
+        if ev is not None:
+            ev[1].record(stream)
+
+    for i in range(args.warmup):
+        step(pools[i % n_pools])
+    torch.cuda.synchronize()
+    if pa.get_device_error() != 0:
+        raise RuntimeError("device error during warm-up")
+
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local) if rank == 0 else None
+    if sampler:
+        time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    start.record(stream)
+    for i in range(args.steps):
+        step(pools[i % n_pools], evs[i])
+    end.record(stream)
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    barrier(world)
+    if sampler:
+        time.sleep(0.3)
+        sampler.stop()
+    ms_total = start.elapsed_time(end)
+    dec_ms = [a.elapsed_time(b) for a, b in evs]
+    dec_avg_ms = sum(dec_ms) / len(dec_ms)
+    err = pa.get_device_error()
+    if err != 0:
+        raise RuntimeError(f"device error word {err:#x} after the timed region")
+
+    # ---------------- end to end through the public API with host buffers
+    p0 = pools[0]
+    host = {k: getattr(p0, k).cpu().pin_memory()
+            for k in ("q", "k_new", "v_new", "slot_mapping", "block_tables", "context_lens")}
+    if fp8:
+        host["k_scale_new"] = p0.k_scale_new.cpu().pin_memory()
+        host["v_scale_new"] = p0.v_scale_new.cpu().pin_memory()
+    dev_in = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
+    out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = out_host.numel() * out_host.element_size()
+
+    def e2e_step(p):
+        for k, v in host.items():
+            dev_in[k].copy_(v, non_blocking=True)
+        pa.store_kv(dev_in["k_new"], dev_in["v_new"], dev_in["slot_mapping"], p.k_cache,
+                    p.v_cache, dev_in.get("k_scale_new"), dev_in.get("v_scale_new"), p.k_scale,
+                    p.v_scale)
+        pa.decode(dev_in["q"], p.k_cache, p.v_cache, dev_in["block_tables"],
+                  dev_in["context_lens"], p.scale, max_context_len=max_len, out=out,
+                  workspace=workspace, k_scale=p.k_scale, v_scale=p.v_scale)
+        out_host.copy_(out, non_blocking=True)
+
+    for _ in range(max(3, args.warmup)):
+        e2e_step(p0)
+    torch.cuda.synchronize()
+    e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    e_start.record(stream)
+    for _ in range(args.steps):
+        e2e_step(p0)  # same pool: the KV cache is resident state, only step inputs move
+    e_end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    e2e_ms = e_start.elapsed_time(e_end)
+
+    ms_total = max_over_ranks(world, ms_total)
+    e2e_ms = max_over_ranks(world, e2e_ms)
+    dec_avg_ms = max_over_ranks(world, dec_avg_ms)
+    total_bytes = sum_over_ranks(world, float(step_bytes)) * args.steps
+    value = total_bytes / (ms_total / 1e3) / 1e9
+    e2e_value = total_bytes / (e2e_ms / 1e3) / 1e9
+
+    if rank != 0:
+        return
+    peak, peak_kind = peaks()
+    achieved = step_bytes / (dec_avg_ms / 1e3) / 1e9
+    traffic = traffic_from_profile("pa_decode.cu", name)
+    n_launch = 1 + 1 + (1 if ws_bytes > 0 else 0)
+    clocks = sampler.summary(t_wall0, t_wall1) if sampler else None
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "fp8_e4m3" if fp8 else "bf16", "data": "synthetic",
+        "config": {"workload": name, "batch": B, "num_heads": w["num_heads"],
+                   "num_kv_heads": w["num_kv_heads"], "head_dim": w["head_dim"],
+                   "block_size": w["block_size"], "kv_dtype": w["kv_dtype"],
+                   "context_len_mean": sum(lens) / len(lens), "context_len_max": max_len,
+                   "kv_bytes_per_step": step_bytes,
+                   "step": "store_kv(new tokens) + decode (split + merge)",
+                   "l2": f"rotating {n_pools} KV pools, {n_pools * step_bytes / 1e9:.2f} GB of KV "
+                         f"between reuses > 129 MB L2",
+                   "parallelism": f"replicas x{world} (sequences sharded, no collective)"},
+        "seq_steps_per_s": B * world * args.steps / (ms_total / 1e3),
+        "us_per_step": ms_total / args.steps * 1e3,
+        "hbm_frac_of_peak": value / peak,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "kernel": "pa_decode (split + merge launches, CUDA events per call)",
+                     "peak_kind": f"of {peak_kind}"},
+        "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": n_launch * args.steps,
+        "clocks": clocks,
+    }
+    if not args.no_cpu_baseline and world == 1:
+        line["cpu_baseline"] = cpu_baseline(name)
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["gpu", "reference"], default="gpu")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
+                    choices=[k for k, v in W.WORKLOADS.items() if v["kind"] == "decode"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world, rank, local = dist_setup(args)
+    try:
+        if args.impl == "reference":
+            run_reference(args, world, rank)
+        else:
+            run_gpu(args, world, rank, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,155 @@
+/*
+ * pa.h - C ABI of the GB300 (sm_103a) paged-KV-cache attention library.
+ *
+ * Three operations, as the source pages define them:
+ *   pa_store_kv        append new tokens' K/V to their cache slots
+ *                      ("tiny-vllm part 05", section "Gathering K/V into a
+ *                      batched buffer and scattering into blocks"; the
+ *                      store_kvcache step of "Decode Phase Attention Forward
+ *                      Pass", section 2).
+ *   pa_decode          one query per sequence attending over exactly
+ *                      context_len cached keys, read through the block table,
+ *                      with GQA head grouping ("Decode Phase Attention Forward
+ *                      Pass", sections 2-4 and the zero-padding caveat;
+ *                      "Decode Phase" glossary, the q.K^T / softmax / sum-of-V
+ *                      steps).
+ *   pa_prefill_varlen  packed varlen prefill over a prefix already in the
+ *                      paged cache, bottom-right-aligned causal mask
+ *                      ("Prefill Forward Prefix Caching Explained", Facts 1-2
+ *                      and the mask section).
+ *
+ * Conventions shared by every call
+ *   - Every tensor pointer is a DEVICE pointer owned by the caller. The
+ *     library never allocates, frees or retains device memory beyond a call
+ *     (split-K scratch is passed in as `workspace`).
+ *   - All calls are asynchronous on `stream` (a cudaStream_t passed as void*;
+ *     NULL = the legacy default stream) and never synchronise the host.
+ *   - Argument errors are returned before anything is launched. A launch
+ *     failure returns PA_ERR_CUDA. Out-of-range indices found on the device
+ *     (a slot beyond the pool, a wait that timed out) never fault: the access
+ *     is skipped and a bit is set in a per-device error word, read with
+ *     pa_get_device_error().
+ *   - Layouts (row-major, contiguous):
+ *       k_cache, v_cache  (num_blocks, block_size, num_kv_heads, head_dim)
+ *                         bf16, or FP8-E4M3 bytes (OCP "e4m3fn");
+ *       k_scale, v_scale  (num_blocks, num_kv_heads, block_size) fp32, FP8
+ *                         only: element = code value * scale;
+ *       block_tables      (batch, max_blocks_per_seq) int32, physical block
+ *                         of logical block j of sequence b;
+ *       slot              physical_block * block_size + offset (int64).
+ *   - Head map (GQA/MQA): query head h reads kv head h / (num_heads /
+ *     num_kv_heads), i.e. the repeat_interleave grouping of the decode page.
+ *   - Supported: head_dim 64 or 128 (FP8: 128), block_size 16 or 32,
+ *     num_heads a multiple of num_kv_heads with at most 8 query heads per kv
+ *     head. Anything else returns PA_ERR_UNSUPPORTED.
+ */
+#ifndef PA_GB300_H
+#define PA_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define PA_ABI_VERSION 1
+
+typedef enum {
+  PA_OK = 0,
+  PA_ERR_NULL = 1,        /* a required pointer is NULL */
+  PA_ERR_SHAPE = 2,       /* a size is negative/zero where it must not be, or inconsistent */
+  PA_ERR_DTYPE = 3,       /* cache dtype / scale pointers do not match */
+  PA_ERR_UNSUPPORTED = 4, /* valid but not implemented (head_dim, block_size, group size) */
+  PA_ERR_CUDA = 5,        /* a CUDA runtime/driver call or a launch failed */
+  PA_ERR_WORKSPACE = 6,   /* workspace missing or smaller than pa_decode_workspace_size() */
+  PA_ERR_ALIGN = 7        /* a pointer is not 16-byte aligned */
+} pa_status;
+
+typedef enum { PA_KV_BF16 = 0, PA_KV_FP8_E4M3 = 1 } pa_kv_dtype;
+
+/* Device error word bits (pa_get_device_error). */
+#define PA_DEVERR_SLOT_RANGE 0x1u   /* store_kv: slot >= num_blocks*block_size, skipped */
+#define PA_DEVERR_WAIT_TIMEOUT 0x2u /* a kernel's bounded wait on a copy gave up */
+#define PA_DEVERR_BLOCK_RANGE 0x4u  /* block table entry outside [0, num_blocks), zero-filled */
+
+/* A paged KV cache (one layer). Pointers are device pointers; the struct
+ * itself is read on the host during the call and may live on the stack. */
+typedef struct {
+  int32_t num_blocks;   /* physical blocks in the pool */
+  int32_t block_size;   /* tokens per block: 16 or 32 */
+  int32_t num_kv_heads;
+  int32_t head_dim;     /* 64 or 128 */
+  int32_t dtype;        /* pa_kv_dtype */
+  void* k_cache;        /* (num_blocks, block_size, num_kv_heads, head_dim) */
+  void* v_cache;
+  float* k_scale;       /* (num_blocks, num_kv_heads, block_size), FP8 only, else NULL */
+  float* v_scale;
+} pa_kv_cache;
+
+/* ABI version of the loaded library (PA_ABI_VERSION it was built with). */
+int32_t pa_abi_version(void);
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* pa_status_string(pa_status status);
+
+/*
+ * pa_store_kv - write num_tokens new K/V rows into the cache.
+ *   k, v           (num_tokens, num_kv_heads, head_dim), cache dtype (bf16, or
+ *                  E4M3 bytes for an FP8 cache), device.
+ *   k_scale_new,   (num_tokens, num_kv_heads) fp32, FP8 caches only (else NULL).
+ *   v_scale_new
+ *   slot_mapping   (num_tokens) int64: destination slot of token t; a negative
+ *                  slot skips the token (padding). Slots within one call must
+ *                  be distinct (otherwise which write wins is unspecified).
+ *   Bytes are copied unchanged (bit-exact). A slot >= num_blocks*block_size is
+ *   skipped and flagged PA_DEVERR_SLOT_RANGE. num_tokens == 0 is a no-op.
+ */
+pa_status pa_store_kv(const void* k, const void* v, const float* k_scale_new,
+                      const float* v_scale_new, const int64_t* slot_mapping, int32_t num_tokens,
+                      const pa_kv_cache* cache, void* stream);
+
+/*
+ * pa_decode_workspace_size - bytes of device scratch pa_decode needs for this
+ * shape (split-K partial results). 0 means pa_decode needs no workspace.
+ * max_context_len is the same host-side bound that will be passed to
+ * pa_decode (<= 0: the block-table capacity max_blocks_per_seq*block_size).
+ */
+size_t pa_decode_workspace_size(const pa_kv_cache* cache, int32_t batch, int32_t num_heads,
+                                int32_t max_blocks_per_seq, int32_t max_context_len);
+
+/*
+ * pa_decode - single-query attention over a paged KV cache.
+ *   q               (batch, num_heads, head_dim) bf16.
+ *   block_tables    (batch, max_blocks_per_seq) int32; only the first
+ *                   ceil(context_len/block_size) entries of a row are read.
+ *   context_lens    (batch) int32 on the device: keys 0..context_len-1 of each
+ *                   sequence are attended (the token stored this step
+ *                   included). context_len 0 gives a zero output row.
+ *   max_context_len host-side upper bound of every context_len (sizes the
+ *                   split-K grid; <= 0 means max_blocks_per_seq*block_size).
+ *                   Keys at positions >= this bound are not attended.
+ *   scale           softmax scale applied to q.k.
+ *   out             (batch, num_heads, head_dim) bf16.
+ *   workspace       device scratch of at least pa_decode_workspace_size()
+ *                   bytes (may be NULL when that is 0). Contents on entry are
+ *                   ignored; calls sharing one workspace must not overlap.
+ * Arithmetic: bf16 (or E4M3 widened exactly to f16) operands, fp32 scores,
+ * softmax and accumulation, one round to bf16 at the output.
+ */
+pa_status pa_decode(const void* q, const pa_kv_cache* cache, const int32_t* block_tables,
+                    int32_t max_blocks_per_seq, const int32_t* context_lens,
+                    int32_t max_context_len, int32_t batch, int32_t num_heads, float scale,
+                    void* out, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * pa_get_device_error - synchronise the current device, return its error word
+ * (PA_DEVERR_* bits, 0 if none) in *code and clear it.
+ */
+pa_status pa_get_device_error(uint32_t* code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_GB300_H */

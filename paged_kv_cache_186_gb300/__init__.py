@@ -1,0 +1,162 @@
+"""Python binding of the sm_103a paged-KV-cache attention library.
+
+Thin ctypes marshalling over the C ABI declared in include/pa.h: tensors are
+passed as device pointers, the stream is torch's current CUDA stream. Every
+step of the computation runs in the library's CUDA kernels; this module never
+computes attention itself and has no fallback. If libpa_gb300.so is missing,
+every call raises (build it with ``python -m paged_kv_cache_186_gb300.build``).
+
+Names follow the C ABI: store_kv, decode, decode_workspace_size,
+get_device_error.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libpa_gb300.so")
+
+PA_KV_BF16 = 0
+PA_KV_FP8_E4M3 = 1
+
+PA_DEVERR_SLOT_RANGE = 0x1
+PA_DEVERR_WAIT_TIMEOUT = 0x2
+PA_DEVERR_BLOCK_RANGE = 0x4
+
+STATUS = {0: "PA_OK", 1: "PA_ERR_NULL", 2: "PA_ERR_SHAPE", 3: "PA_ERR_DTYPE",
+          4: "PA_ERR_UNSUPPORTED", 5: "PA_ERR_CUDA", 6: "PA_ERR_WORKSPACE", 7: "PA_ERR_ALIGN"}
+
+# Every symbol include/pa.h declares.
+EXPORTED = ("pa_abi_version", "pa_status_string", "pa_store_kv", "pa_decode_workspace_size",
+            "pa_decode", "pa_get_device_error")
+
+
+class PAError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        self.code = code
+        super().__init__(f"{what}: {STATUS.get(code, code)}")
+
+
+class KVCache(ctypes.Structure):
+    """Mirror of pa_kv_cache."""
+    _fields_ = [("num_blocks", ctypes.c_int32), ("block_size", ctypes.c_int32),
+                ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("dtype", ctypes.c_int32), ("k_cache", ctypes.c_void_p),
+                ("v_cache", ctypes.c_void_p), ("k_scale", ctypes.c_void_p),
+                ("v_scale", ctypes.c_void_p)]
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load libpa_gb300.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                           "`python -m paged_kv_cache_186_gb300.build` (needs nvcc)")
+    L = ctypes.CDLL(LIB_PATH)
+    P, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+    L.pa_abi_version.restype = i32
+    L.pa_abi_version.argtypes = []
+    L.pa_status_string.restype = ctypes.c_char_p
+    L.pa_status_string.argtypes = [ctypes.c_int]
+    L.pa_store_kv.restype = ctypes.c_int
+    L.pa_store_kv.argtypes = [P, P, P, P, P, i32, ctypes.POINTER(KVCache), P]
+    L.pa_decode_workspace_size.restype = ctypes.c_size_t
+    L.pa_decode_workspace_size.argtypes = [ctypes.POINTER(KVCache), i32, i32, i32, i32]
+    L.pa_decode.restype = ctypes.c_int
+    L.pa_decode.argtypes = [P, ctypes.POINTER(KVCache), P, i32, P, i32, i32, i32, ctypes.c_float,
+                            P, P, ctypes.c_size_t, P]
+    L.pa_get_device_error.restype = ctypes.c_int
+    L.pa_get_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
+    del i64
+    _lib = L
+    return L
+
+
+def _ptr(t: torch.Tensor | None):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream():
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _check(code: int, what: str):
+    if code != 0:
+        raise PAError(code, what)
+
+
+def make_cache(k_cache: torch.Tensor, v_cache: torch.Tensor, k_scale: torch.Tensor | None = None,
+               v_scale: torch.Tensor | None = None) -> KVCache:
+    """Describe caches of shape (num_blocks, block_size, num_kv_heads, head_dim):
+    bf16, or uint8 E4M3 codes with fp32 scales (num_blocks, num_kv_heads, block_size)."""
+    if k_cache.dtype == torch.bfloat16:
+        dt = PA_KV_BF16
+    elif k_cache.dtype in (torch.uint8, torch.float8_e4m3fn):
+        dt = PA_KV_FP8_E4M3
+    else:
+        raise TypeError(f"unsupported cache dtype {k_cache.dtype}")
+    for t in (k_cache, v_cache, k_scale, v_scale):
+        if t is not None and not t.is_contiguous():
+            raise ValueError("cache tensors must be contiguous")
+    nb, bs, hkv, d = k_cache.shape
+    return KVCache(nb, bs, hkv, d, dt, k_cache.data_ptr(), v_cache.data_ptr(),
+                   None if k_scale is None else k_scale.data_ptr(),
+                   None if v_scale is None else v_scale.data_ptr())
+
+
+def store_kv(k, v, slot_mapping, k_cache, v_cache, k_scale_new=None, v_scale_new=None,
+             k_scale=None, v_scale=None) -> None:
+    """pa_store_kv: write k/v (T, Hkv, D) to their slots (int64 (T,)), in place."""
+    cache = make_cache(k_cache, v_cache, k_scale, v_scale)
+    k, v = k.contiguous(), v.contiguous()
+    sm = slot_mapping.contiguous()
+    _check(lib().pa_store_kv(_ptr(k), _ptr(v), _ptr(k_scale_new), _ptr(v_scale_new), _ptr(sm),
+                             int(sm.numel()), ctypes.byref(cache), _stream()), "pa_store_kv")
+
+
+def decode_workspace_size(k_cache, batch: int, num_heads: int, max_blocks_per_seq: int,
+                          max_context_len: int = 0, v_cache=None, k_scale=None,
+                          v_scale=None) -> int:
+    cache = make_cache(k_cache, k_cache if v_cache is None else v_cache, k_scale, v_scale)
+    return int(lib().pa_decode_workspace_size(ctypes.byref(cache), batch, num_heads,
+                                              max_blocks_per_seq, max_context_len))
+
+
+def decode(q, k_cache, v_cache, block_tables, context_lens, scale: float, *,
+           max_context_len: int = 0, out=None, workspace=None, k_scale=None,
+           v_scale=None) -> torch.Tensor:
+    """pa_decode: q (B, H, D) bf16 -> out (B, H, D) bf16.
+
+    max_context_len is the host-side bound of context_lens (0 = block-table
+    capacity). A workspace (uint8 tensor) is allocated when none is given.
+    """
+    cache = make_cache(k_cache, v_cache, k_scale, v_scale)
+    B, H, D = q.shape
+    bt = block_tables.contiguous()
+    cl = context_lens.contiguous()
+    if out is None:
+        out = torch.empty((B, H, D), dtype=torch.bfloat16, device=q.device)
+    need = int(lib().pa_decode_workspace_size(ctypes.byref(cache), B, H, bt.shape[1],
+                                              max_context_len))
+    if need and (workspace is None or workspace.numel() * workspace.element_size() < need):
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().pa_decode(_ptr(q.contiguous()), ctypes.byref(cache), _ptr(bt), bt.shape[1],
+                           _ptr(cl), int(max_context_len), B, H, float(scale), _ptr(out),
+                           _ptr(workspace), ws_bytes, _stream()), "pa_decode")
+    return out
+
+
+def get_device_error() -> int:
+    """Synchronise the device, return and clear its PA_DEVERR_* word."""
+    code = ctypes.c_uint32(0)
+    _check(lib().pa_get_device_error(ctypes.byref(code)), "pa_get_device_error")
+    return int(code.value)

@@ -1,0 +1,253 @@
+// C-ABI entry points: argument validation, tensor-map encoding, launch.
+// Every check happens on the host before any launch; nothing here reads
+// device memory or synchronises (except pa_get_device_error).
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "pa.h"
+#include "pa_launch.h"
+
+namespace {
+
+// Per-device error word (PA_DEVERR_* bits), set by kernels with atomicOr.
+__device__ uint32_t g_device_error;
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+  bool ready = false;
+  uint32_t* err = nullptr;
+  int num_sms = 0;
+};
+
+std::mutex g_mu;
+DeviceInfo g_dev[kMaxDevices];
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+// Resolve per-device state (error-word address, SM count) for the current
+// device; the first call on a device does the lookup.
+pa_status device_info(DeviceInfo** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return PA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.ready) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return PA_ERR_CUDA;
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return PA_ERR_CUDA;
+    d.err = static_cast<uint32_t*>(p);
+    d.num_sms = sms;
+    d.ready = true;
+  }
+  if (g_encode == nullptr) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || fn == nullptr)
+      return PA_ERR_CUDA;
+    g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+  }
+  *out = &d;
+  return PA_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+pa_status check_cache(const pa_kv_cache* c) {
+  if (c == nullptr || c->k_cache == nullptr || c->v_cache == nullptr) return PA_ERR_NULL;
+  if (c->num_blocks <= 0 || c->block_size <= 0 || c->num_kv_heads <= 0 || c->head_dim <= 0)
+    return PA_ERR_SHAPE;
+  if (c->dtype != PA_KV_BF16 && c->dtype != PA_KV_FP8_E4M3) return PA_ERR_DTYPE;
+  const bool fp8 = c->dtype == PA_KV_FP8_E4M3;
+  if (fp8 && (c->k_scale == nullptr || c->v_scale == nullptr)) return PA_ERR_DTYPE;
+  if (!fp8 && (c->k_scale != nullptr || c->v_scale != nullptr)) return PA_ERR_DTYPE;
+  if (c->block_size != 16 && c->block_size != 32) return PA_ERR_UNSUPPORTED;
+  if (fp8 ? c->head_dim != 128 : (c->head_dim != 64 && c->head_dim != 128))
+    return PA_ERR_UNSUPPORTED;
+  if (static_cast<long long>(c->num_blocks) * c->block_size > 0x7fffffffLL) return PA_ERR_SHAPE;
+  if (!aligned16(c->k_cache) || !aligned16(c->v_cache)) return PA_ERR_ALIGN;
+  if (fp8 && (!aligned16(c->k_scale) || !aligned16(c->v_scale))) return PA_ERR_ALIGN;
+  return PA_OK;
+}
+
+int elem_bytes(const pa_kv_cache* c) { return c->dtype == PA_KV_FP8_E4M3 ? 1 : 2; }
+
+// Tensor map over a cache viewed as 3-D (head_dim, num_kv_heads,
+// num_blocks*block_size), boxes of one 128-byte-wide, block_size-tall tile of
+// one kv head, 128B-swizzled (matching the kernels' shared-memory layout).
+pa_status encode_cache_map(CUtensorMap* map, void* base, const pa_kv_cache* c) {
+  const int eb = elem_bytes(c);
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(c->head_dim),
+                              static_cast<cuuint64_t>(c->num_kv_heads),
+                              static_cast<cuuint64_t>(c->num_blocks) * c->block_size};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(c->head_dim) * eb,
+                                 static_cast<cuuint64_t>(c->head_dim) * eb * c->num_kv_heads};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(pa::kSwizzleBytes / eb), 1u,
+                             static_cast<cuuint32_t>(c->block_size)};
+  const cuuint32_t estr[3] = {1u, 1u, 1u};
+  const CUresult r = g_encode(
+      map, eb == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base,
+      dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
+}
+
+int decode_len_cap(const pa_kv_cache* c, int32_t max_blocks_per_seq, int32_t max_context_len) {
+  const long long cap = static_cast<long long>(max_blocks_per_seq) * c->block_size;
+  long long v = max_context_len > 0 ? std::min<long long>(max_context_len, cap) : cap;
+  return static_cast<int>(std::min<long long>(v, 0x7fffffffLL));
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t pa_abi_version(void) { return PA_ABI_VERSION; }
+
+const char* pa_status_string(pa_status s) {
+  switch (s) {
+    case PA_OK: return "ok";
+    case PA_ERR_NULL: return "required pointer is NULL";
+    case PA_ERR_SHAPE: return "invalid or inconsistent size";
+    case PA_ERR_DTYPE: return "cache dtype and scale pointers do not match";
+    case PA_ERR_UNSUPPORTED: return "unsupported head_dim, block_size or head grouping";
+    case PA_ERR_CUDA: return "CUDA call or kernel launch failed";
+    case PA_ERR_WORKSPACE: return "workspace missing or too small";
+    case PA_ERR_ALIGN: return "pointer not 16-byte aligned";
+  }
+  return "unknown status";
+}
+
+pa_status pa_store_kv(const void* k, const void* v, const float* k_scale_new,
+                      const float* v_scale_new, const int64_t* slot_mapping, int32_t num_tokens,
+                      const pa_kv_cache* cache, void* stream) {
+  pa_status st = check_cache(cache);
+  if (st != PA_OK) return st;
+  if (num_tokens < 0) return PA_ERR_SHAPE;
+  if (num_tokens == 0) return PA_OK;
+  if (k == nullptr || v == nullptr || slot_mapping == nullptr) return PA_ERR_NULL;
+  const bool fp8 = cache->dtype == PA_KV_FP8_E4M3;
+  if (fp8 != (k_scale_new != nullptr) || fp8 != (v_scale_new != nullptr)) return PA_ERR_DTYPE;
+  if (!aligned16(k) || !aligned16(v)) return PA_ERR_ALIGN;
+  DeviceInfo* dev = nullptr;
+  if ((st = device_info(&dev)) != PA_OK) return st;
+  pa::StoreArgs a{};
+  a.k = k;
+  a.v = v;
+  a.k_scale_new = k_scale_new;
+  a.v_scale_new = v_scale_new;
+  a.slot_mapping = slot_mapping;
+  a.k_cache = cache->k_cache;
+  a.v_cache = cache->v_cache;
+  a.k_scale = fp8 ? cache->k_scale : nullptr;
+  a.v_scale = fp8 ? cache->v_scale : nullptr;
+  a.num_tokens = num_tokens;
+  a.row_bytes = cache->num_kv_heads * cache->head_dim * elem_bytes(cache);
+  a.num_kv_heads = cache->num_kv_heads;
+  a.block_size = cache->block_size;
+  a.num_slots = static_cast<long long>(cache->num_blocks) * cache->block_size;
+  a.err = dev->err;
+  return pa::launch_store_kv(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PA_OK
+                                                                                  : PA_ERR_CUDA;
+}
+
+size_t pa_decode_workspace_size(const pa_kv_cache* cache, int32_t batch, int32_t num_heads,
+                                int32_t max_blocks_per_seq, int32_t max_context_len) {
+  if (check_cache(cache) != PA_OK || batch <= 0 || num_heads <= 0 || max_blocks_per_seq <= 0)
+    return 0;
+  DeviceInfo* dev = nullptr;
+  if (device_info(&dev) != PA_OK) return 0;
+  const int cap = decode_len_cap(cache, max_blocks_per_seq, max_context_len);
+  return pa::plan_decode(batch, num_heads, cache->num_kv_heads, cache->head_dim, cache->block_size,
+                         cache->dtype == PA_KV_FP8_E4M3, cap, dev->num_sms)
+      .workspace_bytes;
+}
+
+pa_status pa_decode(const void* q, const pa_kv_cache* cache, const int32_t* block_tables,
+                    int32_t max_blocks_per_seq, const int32_t* context_lens,
+                    int32_t max_context_len, int32_t batch, int32_t num_heads, float scale,
+                    void* out, void* workspace, size_t workspace_bytes, void* stream) {
+  pa_status st = check_cache(cache);
+  if (st != PA_OK) return st;
+  if (batch < 0 || num_heads <= 0 || max_blocks_per_seq <= 0) return PA_ERR_SHAPE;
+  if (batch == 0) return PA_OK;
+  if (q == nullptr || block_tables == nullptr || context_lens == nullptr || out == nullptr)
+    return PA_ERR_NULL;
+  if (num_heads % cache->num_kv_heads != 0) return PA_ERR_SHAPE;
+  const int group = num_heads / cache->num_kv_heads;
+  if (group > 8) return PA_ERR_UNSUPPORTED;
+  if (batch > 65535) return PA_ERR_UNSUPPORTED;
+  if (!std::isfinite(scale)) return PA_ERR_SHAPE;
+  if (!aligned16(q) || !aligned16(out)) return PA_ERR_ALIGN;
+  DeviceInfo* dev = nullptr;
+  if ((st = device_info(&dev)) != PA_OK) return st;
+  const int cap = decode_len_cap(cache, max_blocks_per_seq, max_context_len);
+  const bool fp8 = cache->dtype == PA_KV_FP8_E4M3;
+  const pa::DecodePlan plan = pa::plan_decode(batch, num_heads, cache->num_kv_heads,
+                                              cache->head_dim, cache->block_size, fp8, cap,
+                                              dev->num_sms);
+  if (plan.workspace_bytes > 0 &&
+      (workspace == nullptr || workspace_bytes < plan.workspace_bytes || !aligned16(workspace)))
+    return PA_ERR_WORKSPACE;
+  CUtensorMap kmap, vmap;
+  if ((st = encode_cache_map(&kmap, cache->k_cache, cache)) != PA_OK) return st;
+  if ((st = encode_cache_map(&vmap, cache->v_cache, cache)) != PA_OK) return st;
+  pa::DecodeArgs a{};
+  a.q = q;
+  a.block_tables = block_tables;
+  a.context_lens = context_lens;
+  a.k_scale = fp8 ? cache->k_scale : nullptr;
+  a.v_scale = fp8 ? cache->v_scale : nullptr;
+  a.out = out;
+  if (plan.workspace_bytes > 0) {
+    const size_t rows = static_cast<size_t>(batch) * num_heads * plan.num_splits;
+    a.part_o = static_cast<float*>(workspace);
+    a.part_ml = a.part_o + rows * cache->head_dim;
+  }
+  a.err = dev->err;
+  a.batch = batch;
+  a.num_heads = num_heads;
+  a.num_kv_heads = cache->num_kv_heads;
+  a.group = group;
+  a.head_dim = cache->head_dim;
+  a.block_size = cache->block_size;
+  a.max_blocks = max_blocks_per_seq;
+  a.num_blocks = cache->num_blocks;
+  a.len_cap = cap;
+  a.blocks_per_split = plan.blocks_per_split;
+  a.num_splits = plan.num_splits;
+  a.fp8 = fp8;
+  a.scale_log2 = scale * 1.4426950408889634f;  // log2(e): scores kept in base-2 units
+  return pa::launch_decode(a, kmap, vmap, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? PA_OK
+             : PA_ERR_CUDA;
+}
+
+pa_status pa_get_device_error(uint32_t* code) {
+  if (code == nullptr) return PA_ERR_NULL;
+  DeviceInfo* dev = nullptr;
+  pa_status st = device_info(&dev);
+  if (st != PA_OK) return st;
+  if (cudaDeviceSynchronize() != cudaSuccess) return PA_ERR_CUDA;
+  uint32_t v = 0;
+  if (cudaMemcpy(&v, dev->err, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess) return PA_ERR_CUDA;
+  const uint32_t zero = 0;
+  if (cudaMemcpy(dev->err, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess)
+    return PA_ERR_CUDA;
+  *code = v;
+  return PA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,62 @@
+// store_kv: append new tokens' K/V rows to their paged-cache slots.
+//
+// "tiny-vllm part 05", section "Gathering K/V into a batched buffer and
+// scattering into blocks": the token at position p goes to logical block
+// p / BLOCK_SIZE, offset p % BLOCK_SIZE of its sequence; the page's engine
+// does this with two device-to-device copies per token. Here the caller
+// supplies the resolved slot (physical_block * block_size + offset) and one
+// warp moves a token's K and V rows with 16-byte vector accesses, so a whole
+// decode batch (or a prefill chunk) is one launch.
+#include "pa_device.cuh"
+#include "pa_launch.h"
+
+namespace pa {
+
+namespace {
+
+constexpr int kStoreWarps = 4;
+
+__global__ void __launch_bounds__(kStoreWarps * 32) store_kv_kernel(const StoreArgs a) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * kStoreWarps + warp;
+  if (t >= a.num_tokens) return;
+  const long long slot = a.slot_mapping[t];
+  if (slot < 0) return;  // padding token
+  if (slot >= a.num_slots) {
+    if (lane == 0) report_error(a.err, PA_DEVERR_SLOT_RANGE);
+    return;
+  }
+  const int n16 = a.row_bytes >> 4;
+  const uint4* ks = reinterpret_cast<const uint4*>(static_cast<const char*>(a.k) +
+                                                   static_cast<long long>(t) * a.row_bytes);
+  const uint4* vs = reinterpret_cast<const uint4*>(static_cast<const char*>(a.v) +
+                                                   static_cast<long long>(t) * a.row_bytes);
+  uint4* kd = reinterpret_cast<uint4*>(static_cast<char*>(a.k_cache) + slot * a.row_bytes);
+  uint4* vd = reinterpret_cast<uint4*>(static_cast<char*>(a.v_cache) + slot * a.row_bytes);
+  for (int i = lane; i < n16; i += 32) {
+    const uint4 kv = __ldg(ks + i);
+    const uint4 vv = __ldg(vs + i);
+    kd[i] = kv;
+    vd[i] = vv;
+  }
+  if (a.k_scale != nullptr) {
+    // scales: new (T, Hkv) -> cache (num_blocks, Hkv, block_size)
+    const long long blk = slot / a.block_size, off = slot % a.block_size;
+    for (int h = lane; h < a.num_kv_heads; h += 32) {
+      const long long dst = (blk * a.num_kv_heads + h) * a.block_size + off;
+      a.k_scale[dst] = a.k_scale_new[static_cast<long long>(t) * a.num_kv_heads + h];
+      a.v_scale[dst] = a.v_scale_new[static_cast<long long>(t) * a.num_kv_heads + h];
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_store_kv(const StoreArgs& a, cudaStream_t stream) {
+  if (a.num_tokens <= 0) return cudaSuccess;
+  const int grid = (a.num_tokens + kStoreWarps - 1) / kStoreWarps;
+  store_kv_kernel<<<grid, kStoreWarps * 32, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace pa

@@ -275,8 +275,17 @@ def make_prefill(batch: int, num_heads: int, num_kv_heads: int, head_dim: int, b
         meta=dict(cached=cached, q_lens=qls, kv_lens=kv, num_blocks=num_blocks, seed=seed))
 
 
-def make_workload(name: str, device="cpu"):
-    """Inputs of one of the named workloads, at full size."""
+def workload_lengths(name: str) -> list[int]:
+    """The context lengths a decode workload draws (cheap: no tensors)."""
+    w = WORKLOADS[name]
+    if "context_lens" in w:
+        return list(w["context_lens"])
+    return draw_lengths(w["lens"], w["batch"], _gen(w["seed"], "cpu"))
+
+
+def make_workload(name: str, device="cpu", variant: int = 0):
+    """Inputs of one of the named workloads, at full size. `variant` > 0 draws
+    another set of values (same lengths and shapes) for rotating buffers."""
     w = dict(WORKLOADS[name])
     kind = w.pop("kind")
     seed = w.pop("seed")
@@ -287,15 +296,15 @@ def make_workload(name: str, device="cpu"):
         if lens is None:
             lens = draw_lengths(spec, w["batch"], g_cpu)
         return make_decode(w.pop("batch"), w.pop("num_heads"), w.pop("num_kv_heads"),
-                           w.pop("head_dim"), w.pop("block_size"), lens, seed=seed + 7,
-                           device=device, **w)
+                           w.pop("head_dim"), w.pop("block_size"), lens,
+                           seed=seed + 7 + 7919 * variant, device=device, **w)
     cached = torch.randint(w["cached"][0], w["cached"][1] + 1, (w["batch"],),
                            generator=g_cpu).tolist()
     qls = torch.randint(w["q_lens"][0], w["q_lens"][1] + 1, (w["batch"],),
                         generator=g_cpu).tolist()
     return make_prefill(w["batch"], w["num_heads"], w["num_kv_heads"], w["head_dim"],
-                        w["block_size"], cached, qls, pool_factor=w["pool_factor"], seed=seed + 7,
-                        device=device, scale=w["scale"])
+                        w["block_size"], cached, qls, pool_factor=w["pool_factor"],
+                        seed=seed + 7 + 7919 * variant, device=device, scale=w["scale"])
 
 
 def bf16_bits(t: torch.Tensor):
