@@ -20,8 +20,8 @@
  *
  * Conventions shared by every call
  *   - Every tensor pointer is a DEVICE pointer owned by the caller. The
- *     library never allocates, frees or retains device memory beyond a call
- *     (split-K scratch is passed in as `workspace`).
+ *     library never calls a device allocator: pa_decode's split-K scratch is
+ *     passed in as `workspace` (pa_decode_noalloc uses a static buffer).
  *   - All calls are asynchronous on `stream` (a cudaStream_t passed as void*;
  *     NULL = the legacy default stream) and never synchronise the host.
  *   - Argument errors are returned before anything is launched. A launch
@@ -63,7 +63,9 @@ typedef enum {
   PA_ERR_UNSUPPORTED = 4, /* valid but not implemented (head_dim, block_size, group size) */
   PA_ERR_CUDA = 5,        /* a CUDA runtime/driver call or a launch failed */
   PA_ERR_WORKSPACE = 6,   /* workspace missing or smaller than pa_decode_workspace_size() */
-  PA_ERR_ALIGN = 7        /* a pointer is not 16-byte aligned */
+  PA_ERR_ALIGN = 7,       /* a pointer is not 16-byte aligned */
+  PA_ERR_TOO_LARGE = 8    /* pa_decode_noalloc: the shape needs more scratch than the
+                             library's static buffer holds */
 } pa_status;
 
 typedef enum { PA_KV_BF16 = 0, PA_KV_FP8_E4M3 = 1 } pa_kv_dtype;
@@ -141,6 +143,31 @@ pa_status pa_decode(const void* q, const pa_kv_cache* cache, const int32_t* bloc
                     int32_t max_blocks_per_seq, const int32_t* context_lens,
                     int32_t max_context_len, int32_t batch, int32_t num_heads, float scale,
                     void* out, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * pa_decode_noalloc - pa_decode for callers that cannot allocate device memory.
+ * The pages have no counterpart: this entry point exists for callers with no
+ * device allocator of their own (a plain C host program handed device
+ * pointers by another runtime) or whose device memory is fully reserved (a
+ * serving engine's KV-block pool), for whom a scratch cudaMalloc is not an
+ * option. Same arguments and result as pa_decode, minus the workspace: the
+ * split-K scratch is a static device buffer of
+ * PA_DECODE_NOALLOC_SCRATCH_BYTES inside the library, held by every GPU that
+ * loads it until the process exits. Allocates nothing per call (no cudaMalloc,
+ * cudaFree or allocating library routine).
+ *   - Shapes whose pa_decode_workspace_size() exceeds the buffer are rejected
+ *     with PA_ERR_TOO_LARGE before anything is launched.
+ *   - The first call on a device (with it current) looks up the buffer's
+ *     device address; make that first call before any stream capture.
+ *   - All calls share the buffer and it keeps the last call's contents (the
+ *     kernels write every partial they read, so nothing needs clearing). Calls
+ *     that may overlap on the GPU race on it: serialise them.
+ */
+#define PA_DECODE_NOALLOC_SCRATCH_BYTES (32u << 20) /* 32 MiB */
+pa_status pa_decode_noalloc(const void* q, const pa_kv_cache* cache, const int32_t* block_tables,
+                            int32_t max_blocks_per_seq, const int32_t* context_lens,
+                            int32_t max_context_len, int32_t batch, int32_t num_heads,
+                            float scale, void* out, void* stream);
 
 /*
  * pa_get_device_error - synchronise the current device, return its error word

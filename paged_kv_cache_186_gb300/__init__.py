@@ -27,11 +27,15 @@ PA_DEVERR_WAIT_TIMEOUT = 0x2
 PA_DEVERR_BLOCK_RANGE = 0x4
 
 STATUS = {0: "PA_OK", 1: "PA_ERR_NULL", 2: "PA_ERR_SHAPE", 3: "PA_ERR_DTYPE",
-          4: "PA_ERR_UNSUPPORTED", 5: "PA_ERR_CUDA", 6: "PA_ERR_WORKSPACE", 7: "PA_ERR_ALIGN"}
+          4: "PA_ERR_UNSUPPORTED", 5: "PA_ERR_CUDA", 6: "PA_ERR_WORKSPACE", 7: "PA_ERR_ALIGN",
+          8: "PA_ERR_TOO_LARGE"}
+
+# Size of the static scratch buffer pa_decode_noalloc uses (PA_DECODE_NOALLOC_SCRATCH_BYTES).
+DECODE_NOALLOC_SCRATCH_BYTES = 32 << 20
 
 # Every symbol include/pa.h declares.
 EXPORTED = ("pa_abi_version", "pa_status_string", "pa_store_kv", "pa_decode_workspace_size",
-            "pa_decode", "pa_get_device_error")
+            "pa_decode", "pa_decode_noalloc", "pa_get_device_error")
 
 
 class PAError(RuntimeError):
@@ -73,6 +77,9 @@ def lib() -> ctypes.CDLL:
     L.pa_decode.restype = ctypes.c_int
     L.pa_decode.argtypes = [P, ctypes.POINTER(KVCache), P, i32, P, i32, i32, i32, ctypes.c_float,
                             P, P, ctypes.c_size_t, P]
+    L.pa_decode_noalloc.restype = ctypes.c_int
+    L.pa_decode_noalloc.argtypes = [P, ctypes.POINTER(KVCache), P, i32, P, i32, i32, i32,
+                                    ctypes.c_float, P, P]
     L.pa_get_device_error.restype = ctypes.c_int
     L.pa_get_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
     del i64
@@ -152,6 +159,24 @@ def decode(q, k_cache, v_cache, block_tables, context_lens, scale: float, *,
     _check(lib().pa_decode(_ptr(q.contiguous()), ctypes.byref(cache), _ptr(bt), bt.shape[1],
                            _ptr(cl), int(max_context_len), B, H, float(scale), _ptr(out),
                            _ptr(workspace), ws_bytes, _stream()), "pa_decode")
+    return out
+
+
+def decode_noalloc(q, k_cache, v_cache, block_tables, context_lens, scale: float, *,
+                   max_context_len: int = 0, out=None, k_scale=None,
+                   v_scale=None) -> torch.Tensor:
+    """pa_decode_noalloc: pa_decode with the split-K scratch taken from the
+    library's static device buffer instead of a caller workspace. For callers
+    that cannot allocate device memory; `out` should then be passed in."""
+    cache = make_cache(k_cache, v_cache, k_scale, v_scale)
+    B, H, D = q.shape
+    bt = block_tables.contiguous()
+    cl = context_lens.contiguous()
+    if out is None:
+        out = torch.empty((B, H, D), dtype=torch.bfloat16, device=q.device)
+    _check(lib().pa_decode_noalloc(_ptr(q.contiguous()), ctypes.byref(cache), _ptr(bt),
+                                   bt.shape[1], _ptr(cl), int(max_context_len), B, H,
+                                   float(scale), _ptr(out), _stream()), "pa_decode_noalloc")
     return out
 
 

@@ -126,6 +126,7 @@ const char* pa_status_string(pa_status s) {
     case PA_ERR_CUDA: return "CUDA call or kernel launch failed";
     case PA_ERR_WORKSPACE: return "workspace missing or too small";
     case PA_ERR_ALIGN: return "pointer not 16-byte aligned";
+    case PA_ERR_TOO_LARGE: return "shape needs more scratch than the static buffer holds";
   }
   return "unknown status";
 }
