@@ -145,6 +145,33 @@ pa_status pa_decode(const void* q, const pa_kv_cache* cache, const int32_t* bloc
                     void* out, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * pa_prefill_varlen - prefill attention of packed new tokens over their
+ * sequences' paged K/V (cached prefix + the new tokens, which must already be
+ * stored with pa_store_kv), with the bottom-right-aligned causal mask: query
+ * row i of a sequence (0-based) sees keys j <= i + (kv_len - q_len).
+ *   q               (total_q, num_heads, head_dim) bf16, sequences packed.
+ *   block_tables    (batch, max_blocks_per_seq) int32.
+ *   cu_seqlens_q    (batch+1) int32 on the device, prefix sums of q_len
+ *                   (cu_seqlens_q[0] = 0, cu_seqlens_q[batch] = total_q).
+ *   cu_seqlens_k    (batch+1) int32 on the device, prefix sums of kv_len.
+ *   total_q         packed rows of q/out (host-side).
+ *   max_q_len       host-side bound of every q_len (sizes the grid; <= 0 means
+ *                   total_q). Rows past this bound are not computed.
+ *   scale           softmax scale, > 0.
+ *   out             (total_q, num_heads, head_dim) bf16.
+ * A sequence with q_len > kv_len is invalid input: its cached length is taken
+ * as 0 and keys are clamped to kv_len. Supported: bf16 cache, head_dim 128,
+ * block_size 16 or 32, num_heads/num_kv_heads in {1, 2, 4, 8, 16}.
+ * Arithmetic: bf16 operands on the tensor cores, fp32 scores and
+ * accumulation, probabilities rounded to bf16 for P.V, bf16 output.
+ */
+pa_status pa_prefill_varlen(const void* q, const pa_kv_cache* cache, const int32_t* block_tables,
+                            int32_t max_blocks_per_seq, const int32_t* cu_seqlens_q,
+                            const int32_t* cu_seqlens_k, int32_t batch, int32_t num_heads,
+                            int32_t total_q, int32_t max_q_len, float scale, void* out,
+                            void* stream);
+
+/*
  * pa_decode_noalloc - pa_decode for callers that cannot allocate device memory.
  * The pages have no counterpart: this entry point exists for callers with no
  * device allocator of their own (a plain C host program handed device

@@ -6,8 +6,8 @@ step of the computation runs in the library's CUDA kernels; this module never
 computes attention itself and has no fallback. If libpa_gb300.so is missing,
 every call raises (build it with ``python -m paged_kv_cache_186_gb300.build``).
 
-Names follow the C ABI: store_kv, decode, decode_workspace_size,
-get_device_error.
+Names follow the C ABI: store_kv, decode, decode_workspace_size, prefill_varlen,
+decode_noalloc, get_device_error.
 """
 from __future__ import annotations
 
@@ -35,7 +35,7 @@ DECODE_NOALLOC_SCRATCH_BYTES = 32 << 20
 
 # Every symbol include/pa.h declares.
 EXPORTED = ("pa_abi_version", "pa_status_string", "pa_store_kv", "pa_decode_workspace_size",
-            "pa_decode", "pa_decode_noalloc", "pa_get_device_error")
+            "pa_decode", "pa_prefill_varlen", "pa_decode_noalloc", "pa_get_device_error")
 
 
 class PAError(RuntimeError):
@@ -77,6 +77,9 @@ def lib() -> ctypes.CDLL:
     L.pa_decode.restype = ctypes.c_int
     L.pa_decode.argtypes = [P, ctypes.POINTER(KVCache), P, i32, P, i32, i32, i32, ctypes.c_float,
                             P, P, ctypes.c_size_t, P]
+    L.pa_prefill_varlen.restype = ctypes.c_int
+    L.pa_prefill_varlen.argtypes = [P, ctypes.POINTER(KVCache), P, i32, P, P, i32, i32, i32, i32,
+                                    ctypes.c_float, P, P]
     L.pa_decode_noalloc.restype = ctypes.c_int
     L.pa_decode_noalloc.argtypes = [P, ctypes.POINTER(KVCache), P, i32, P, i32, i32, i32,
                                     ctypes.c_float, P, P]
@@ -159,6 +162,24 @@ def decode(q, k_cache, v_cache, block_tables, context_lens, scale: float, *,
     _check(lib().pa_decode(_ptr(q.contiguous()), ctypes.byref(cache), _ptr(bt), bt.shape[1],
                            _ptr(cl), int(max_context_len), B, H, float(scale), _ptr(out),
                            _ptr(workspace), ws_bytes, _stream()), "pa_decode")
+    return out
+
+
+def prefill_varlen(q, k_cache, v_cache, block_tables, cu_seqlens_q, cu_seqlens_k,
+                   scale: float, *, max_q_len: int = 0, out=None) -> torch.Tensor:
+    """pa_prefill_varlen: packed q (total_q, H, D) bf16 -> out (total_q, H, D) bf16,
+    attending over each sequence's paged K/V with the bottom-right causal mask.
+    The new tokens' K/V must already be in the cache (store_kv)."""
+    cache = make_cache(k_cache, v_cache)
+    T, H, D = q.shape
+    bt = block_tables.contiguous()
+    cq, ck = cu_seqlens_q.contiguous(), cu_seqlens_k.contiguous()
+    if out is None:
+        out = torch.empty((T, H, D), dtype=torch.bfloat16, device=q.device)
+    _check(lib().pa_prefill_varlen(_ptr(q.contiguous()), ctypes.byref(cache), _ptr(bt),
+                                   bt.shape[1], _ptr(cq), _ptr(ck), cq.numel() - 1, H, T,
+                                   int(max_q_len), float(scale), _ptr(out), _stream()),
+           "pa_prefill_varlen")
     return out
 
 

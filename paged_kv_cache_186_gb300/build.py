@@ -52,7 +52,7 @@ def build(force: bool = False, verbose_ptxas: bool = False, jobs: int | None = N
     os.makedirs(BUILD, exist_ok=True)
     nvcc = _nvcc()
     common = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE,
-                     "-I", CSRC]
+                     "-I", CSRC, "-diag-suppress", "177"]
     if verbose_ptxas:
         common += ["-Xptxas", "-v"]
 

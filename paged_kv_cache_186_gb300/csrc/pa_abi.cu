@@ -10,6 +10,7 @@
 
 #include "pa.h"
 #include "pa_launch.h"
+#include "pa_prefill.h"
 
 namespace {
 
@@ -232,6 +233,69 @@ pa_status pa_decode(const void* q, const pa_kv_cache* cache, const int32_t* bloc
   a.fp8 = fp8;
   a.scale_log2 = scale * 1.4426950408889634f;  // log2(e): scores kept in base-2 units
   return pa::launch_decode(a, kmap, vmap, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? PA_OK
+             : PA_ERR_CUDA;
+}
+
+pa_status pa_prefill_varlen(const void* q, const pa_kv_cache* cache, const int32_t* block_tables,
+                            int32_t max_blocks_per_seq, const int32_t* cu_seqlens_q,
+                            const int32_t* cu_seqlens_k, int32_t batch, int32_t num_heads,
+                            int32_t total_q, int32_t max_q_len, float scale, void* out,
+                            void* stream) {
+  pa_status st = check_cache(cache);
+  if (st != PA_OK) return st;
+  if (batch < 0 || num_heads <= 0 || total_q < 0 || max_blocks_per_seq <= 0) return PA_ERR_SHAPE;
+  if (batch == 0 || total_q == 0) return PA_OK;
+  if (q == nullptr || block_tables == nullptr || cu_seqlens_q == nullptr ||
+      cu_seqlens_k == nullptr || out == nullptr)
+    return PA_ERR_NULL;
+  if (num_heads % cache->num_kv_heads != 0) return PA_ERR_SHAPE;
+  const int group = num_heads / cache->num_kv_heads;
+  if (cache->dtype != PA_KV_BF16 || cache->head_dim != 128) return PA_ERR_UNSUPPORTED;
+  if (group != 1 && group != 2 && group != 4 && group != 8 && group != 16)
+    return PA_ERR_UNSUPPORTED;
+  if (batch > 65535 || cache->num_kv_heads > 65535) return PA_ERR_UNSUPPORTED;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return PA_ERR_SHAPE;
+  if (!aligned16(q) || !aligned16(out)) return PA_ERR_ALIGN;
+  DeviceInfo* dev = nullptr;
+  if ((st = device_info(&dev)) != PA_OK) return st;
+  const int tpt = pa::prefill_tokens_per_tile(group);
+  const int qbound = max_q_len > 0 ? std::min(max_q_len, total_q) : total_q;
+  // Q viewed as (head_dim, num_heads, total_q); one box = the G heads of a kv
+  // head for tpt consecutive tokens, 64 dims (128 bytes) wide.
+  CUtensorMap qmap, kmap, vmap;
+  {
+    const cuuint64_t dims[3] = {128u, static_cast<cuuint64_t>(num_heads),
+                                static_cast<cuuint64_t>(total_q)};
+    const cuuint64_t strides[2] = {128u * 2u, static_cast<cuuint64_t>(num_heads) * 128u * 2u};
+    const cuuint32_t box[3] = {64u, static_cast<cuuint32_t>(group), static_cast<cuuint32_t>(tpt)};
+    const cuuint32_t estr[3] = {1u, 1u, 1u};
+    if (g_encode(&qmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides,
+                 box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return PA_ERR_CUDA;
+  }
+  if ((st = encode_cache_map(&kmap, cache->k_cache, cache)) != PA_OK) return st;
+  if ((st = encode_cache_map(&vmap, cache->v_cache, cache)) != PA_OK) return st;
+  pa::PrefillArgs a{};
+  a.block_tables = block_tables;
+  a.cu_q = cu_seqlens_q;
+  a.cu_k = cu_seqlens_k;
+  a.out = out;
+  a.err = dev->err;
+  a.batch = batch;
+  a.num_heads = num_heads;
+  a.num_kv_heads = cache->num_kv_heads;
+  a.group = group;
+  a.head_dim = cache->head_dim;
+  a.block_size = cache->block_size;
+  a.max_blocks = max_blocks_per_seq;
+  a.num_blocks = cache->num_blocks;
+  a.tokens_per_tile = tpt;
+  a.num_qtiles = (qbound + tpt - 1) / tpt;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  return pa::launch_prefill(a, qmap, kmap, vmap, static_cast<cudaStream_t>(stream)) == cudaSuccess
              ? PA_OK
              : PA_ERR_CUDA;
 }
