@@ -48,19 +48,36 @@ def kv_bytes(name: str, lens) -> int:
     return int(sum(lens)) * per_tok
 
 
-def peaks():
+def _measured(keys):
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
         with open(path) as f:
             d = json.load(f)
-        hbm = d.get("hbm_gbs") or d.get("hbm_GBps") or d.get("hbm")
-        if isinstance(hbm, dict):
-            hbm = hbm.get("value")
-        if hbm:
-            return float(hbm), "measured"
     except (OSError, ValueError):
-        pass
-    return FALLBACK_HBM_GBS, "fallback"
+        return None
+    for k in keys:
+        v = d.get(k)
+        if isinstance(v, dict):
+            v = v.get("value")
+        if v:
+            return float(v)
+    return None
+
+
+def peaks():
+    hbm = _measured(("hbm_gbs", "hbm_GBps", "hbm"))
+    return (hbm, "measured") if hbm else (FALLBACK_HBM_GBS, "fallback")
+
+
+def tensor_peak():
+    tf = _measured(("bf16_tflops", "bf16_TFLOPs"))
+    return (tf, "measured") if tf else (FALLBACK_BF16_TFLOPS, "fallback")
+
+
+def prefill_flops(cached, q_lens, num_heads, head_dim) -> int:
+    """4 * D * H * sum over query rows of the keys each row sees (Q.K^T and P.V)."""
+    keys = sum(ql * c + ql * (ql + 1) // 2 for c, ql in zip(cached, q_lens))
+    return 4 * head_dim * num_heads * keys
 
 
 def traffic_from_profile(kernel_file: str, workload: str):
@@ -425,21 +442,113 @@ def run_gpu(args, world, rank, local):
     print(json.dumps(line), flush=True)
 
 
+def run_prefill(args, world, rank, local):
+    """Varlen prefill step: store_kv of the new tokens + pa_prefill_varlen."""
+    import paged_kv_cache_186_gb300 as pa
+    from paged_kv_cache_186_gb300 import build as pabuild
+    if rank == 0 or world == 1:
+        pabuild.build()
+    barrier(world)
+    name = args.workload
+    w = W.WORKLOADS[name]
+    dev = torch.device("cuda", torch.cuda.current_device())
+    pools = [W.make_workload(name, device=dev, variant=v + 97 * rank) for v in range(3)]
+    m = pools[0].meta
+    flops = prefill_flops(m["cached"], m["q_lens"], w["num_heads"], w["head_dim"])
+    max_q = max(m["q_lens"])
+    total_q = sum(m["q_lens"])
+    out = torch.empty((total_q, w["num_heads"], w["head_dim"]), dtype=torch.bfloat16, device=dev)
+    # L2 flush buffer: the K/V of one step (~52 MB) fits in L2, so flush between steps
+    flush = torch.empty(256 * 2 ** 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(p):
+        pa.store_kv(p.k_new, p.v_new, p.slot_mapping, p.k_cache, p.v_cache)
+        pa.prefill_varlen(p.q, p.k_cache, p.v_cache, p.block_tables, p.cu_seqlens_q,
+                          p.cu_seqlens_k, p.scale, max_q_len=max_q, out=out)
+
+    for i in range(args.warmup):
+        step(pools[i % 3])
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    pev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    sampler = ClockSampler(local) if rank == 0 else None
+    if sampler:
+        time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    for i in range(args.steps):
+        flush.zero_()  # outside the timed events: write > L2 between steps
+        p = pools[i % 3]
+        evs[i][0].record(stream)
+        pa.store_kv(p.k_new, p.v_new, p.slot_mapping, p.k_cache, p.v_cache)
+        pev[i][0].record(stream)
+        pa.prefill_varlen(p.q, p.k_cache, p.v_cache, p.block_tables, p.cu_seqlens_q,
+                          p.cu_seqlens_k, p.scale, max_q_len=max_q, out=out)
+        pev[i][1].record(stream)
+        evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    barrier(world)
+    if sampler:
+        time.sleep(0.3)
+        sampler.stop()
+    if pa.get_device_error() != 0:
+        raise RuntimeError("device error word set after the timed region")
+    step_ms = sum(a.elapsed_time(b) for a, b in evs) / args.steps
+    pre_ms = sum(a.elapsed_time(b) for a, b in pev) / args.steps
+    step_ms = max_over_ranks(world, step_ms)
+    pre_ms = max_over_ranks(world, pre_ms)
+    total_flops = sum_over_ranks(world, float(flops))
+    if rank != 0:
+        return
+    peak, kind = tensor_peak()
+    achieved = flops / (pre_ms / 1e3) / 1e12
+    line = {
+        "metric": "Varlen prefix-cached prefill attention TFLOP/s", "value":
+            total_flops / (step_ms / 1e3) / 1e12, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": name, "batch": w["batch"], "num_heads": w["num_heads"],
+                   "num_kv_heads": w["num_kv_heads"], "head_dim": w["head_dim"],
+                   "block_size": w["block_size"], "q_lens": m["q_lens"], "cached": m["cached"],
+                   "total_q": total_q, "flops_per_step": flops,
+                   "step": "store_kv(new tokens) + prefill_varlen",
+                   "l2": "256 MB buffer written between timed steps (outside the events)"},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": None,
+                     "kernel": "prefill_kernel (CUDA events per call)",
+                     "peak_kind": f"of {kind} (bf16 dense)"},
+        "gpu_launches": 2 * args.steps,
+        "clocks": sampler.summary(t_wall0, t_wall1) if sampler else None,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["gpu", "reference"], default="gpu")
-    ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
-                    choices=[k for k, v in W.WORKLOADS.items() if v["kind"] == "decode"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(W.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     world, rank, local = dist_setup(args)
     try:
-        if args.impl == "reference":
+        if W.WORKLOADS[args.workload]["kind"] == "prefill":
+            if args.impl == "reference":
+                print(json.dumps({"impl": "reference", "unavailable":
+                                  "the reference arm times the decode workloads only"}))
+            else:
+                run_prefill(args, world, rank, local)
+        elif args.impl == "reference":
             run_reference(args, world, rank)
         else:
             run_gpu(args, world, rank, local)
