@@ -214,9 +214,12 @@ pa_status pa_decode(const void* q, const pa_kv_cache* cache, const int32_t* bloc
   a.v_scale = fp8 ? cache->v_scale : nullptr;
   a.out = out;
   if (plan.workspace_bytes > 0) {
-    const size_t rows = static_cast<size_t>(batch) * num_heads * plan.num_splits;
+    const size_t slots = plan.persistent_ctas > 0
+                             ? 2 * static_cast<size_t>(plan.persistent_ctas)
+                             : static_cast<size_t>(batch) * cache->num_kv_heads * plan.num_splits;
     a.part_o = static_cast<float*>(workspace);
-    a.part_ml = a.part_o + rows * cache->head_dim;
+    a.part_ml = a.part_o + slots * 8 * cache->head_dim;
+    a.prefix_out = reinterpret_cast<int*>(a.part_ml + slots * 8 * 2);
   }
   a.err = dev->err;
   a.batch = batch;
@@ -228,6 +231,7 @@ pa_status pa_decode(const void* q, const pa_kv_cache* cache, const int32_t* bloc
   a.max_blocks = max_blocks_per_seq;
   a.num_blocks = cache->num_blocks;
   a.len_cap = cap;
+  a.persistent_ctas = plan.persistent_ctas;
   a.blocks_per_split = plan.blocks_per_split;
   a.num_splits = plan.num_splits;
   a.fp8 = fp8;

@@ -9,26 +9,31 @@
 // context_len keys take part (no padding to a batch maximum).
 //
 // How (GB300 design):
-//   * Grid = (kv head, sequence, split). A split is a run of consecutive
-//     logical blocks of one sequence (flash-decoding); a CTA's warps take its
-//     blocks round-robin, and all G = H/Hkv query heads of the kv head share
-//     every K/V tile (GQA).
-//   * Each warp streams its physical blocks through a private ring of
-//     shared-memory stages filled by TMA (3-D tiled loads of one block of one
-//     kv head, 128B-swizzled; FP8 scales by 1-D bulk copies), completion
-//     tracked by mbarriers. The block table entries of a warp's blocks are
-//     loaded once up front.
+//   * Work is the list of (sequence, kv head) "segments", each a run of
+//     ceil(context_len / bs) physical blocks. The persistent kernel gives every
+//     CTA an equal contiguous share of all blocks of all segments (a balanced
+//     split: long and short sequences cost the same per block, and no CTA is
+//     launched without work). A segment that straddles CTAs is finished by a
+//     small merge kernel from at most two partial results per CTA.
+//   * A CTA's warps take the blocks of each segment piece round-robin; all
+//     G = H/Hkv query heads of the kv head share every K/V tile (GQA).
+//   * Each warp streams its blocks through a private ring of shared-memory
+//     stages filled by TMA (3-D tiled loads of one block of one kv head,
+//     128B-swizzled; FP8 scales by 1-D bulk copies), tracked by mbarriers with
+//     bounded waits. Loads run ahead across segment boundaries, and the block
+//     id of the next load is fetched one step early to hide its latency.
 //   * The two contractions per block, S = Q K^T (heads x tokens over head_dim)
 //     and O^T += V^T P^T (head_dim x heads over tokens), run on the warp-level
 //     tensor-core MMA (m16n8k16, fp32 accumulate). The softmax is online
 //     ("tiny-vllm part 05", pagedAttentionKernel section): a running max and
 //     sum per head, reduced over the 4 lanes that share a head with warp
 //     shuffles, accumulators rescaled when the max grows.
-//   * Warps of a CTA merge their (max, sum, O) in shared memory; a sequence
-//     that fits one split writes bf16 output directly, otherwise partials go
-//     to the workspace and a second kernel merges the splits (log-sum-exp).
+//   * At the end of each segment piece the warps merge (max, sum, O) in shared
+//     memory; a segment that lies inside one CTA writes bf16 output directly.
 //   * FP8-E4M3 KV: codes are widened exactly to f16 in registers; the K scale
 //     multiplies the score, the V scale multiplies the probability.
+//   * Batches above kMaxPersistentBatch use a grid of (kv head, sequence,
+//     split) CTAs instead, with the same per-block code.
 #include <algorithm>
 #include <cstdlib>
 
@@ -44,21 +49,20 @@ constexpr unsigned kFull = 0xffffffffu;
 template <int D, int BS, int NW, int ST, bool FP8>
 struct Cfg {
   static constexpr int kElem = FP8 ? 1 : 2;
-  static constexpr int kRowBytes = D * kElem;          // one (token, kv head) row
-  static constexpr int kNSub = kRowBytes / kSwizzleBytes;  // 128-byte-wide subtiles per row
+  static constexpr int kRowBytes = D * kElem;                  // one (token, kv head) row
+  static constexpr int kNSub = kRowBytes / kSwizzleBytes;      // 128-byte-wide subtiles per row
   static constexpr int kSubBytes = BS * kSwizzleBytes;
-  static constexpr int kTile = kNSub * kSubBytes;      // K (or V) of one block, one kv head
+  static constexpr int kTile = kNSub * kSubBytes;              // K (or V) of one block, one kv head
   static constexpr int kStage = 2 * kTile;
   static constexpr int kTiles = NW * ST * kStage;
   static constexpr int kScaleBytes = FP8 ? NW * ST * 2 * BS * 4 : 0;
-  static constexpr int kMoStride = D + 4;              // padded row of the merge buffer
+  static constexpr int kMoStride = D + 4;                      // padded row of the merge buffer
   static constexpr int kMerge = NW * 8 * kMoStride * 4 + NW * 8 * 2 * 4;
-  static constexpr int kRegion = ((kTiles > kMerge ? kTiles : kMerge) + 1023) / 1024 * 1024;
-  static constexpr int kSmem = 1024 + kRegion + kScaleBytes;
   static constexpr uint32_t kTx = kStage + (FP8 ? 2 * BS * 4 : 0);
   static_assert(kRowBytes % kSwizzleBytes == 0, "row must be a multiple of 128 bytes");
   static_assert(BS % 16 == 0, "block size must be a multiple of 16");
   static_assert(!FP8 || D == 128, "FP8 path is written for head_dim 128");
+  static_assert(kMerge % 16 == 0, "merge buffer must keep 16-byte alignment");
 };
 
 // Shared-memory byte address of 16-byte chunk `chunk` (0 .. D*elem/16-1) of
@@ -69,6 +73,525 @@ __device__ __forceinline__ uint32_t swz(uint32_t tile, int row, int chunk) {
   return tile + sub * (BS * kSwizzleBytes) + row * kSwizzleBytes + ((c ^ (row & 7)) << 4);
 }
 
+// Q fragments (A operand of S = Q K^T) of kv head `kvh` of sequence b:
+// MMA row r = head r of the group (rows >= G are zero).
+// bf16: k index of step ks = head_dim ks*16 + {2q4, 2q4+1, 2q4+8, 2q4+9}.
+// FP8 (f16 MMA): the head_dim order inside a step is permuted to match how
+// the K codes are read (lane quad q4 owns dims [32 q4, 32 q4 + 32)): step ks
+// uses dims 32 q4 + 4 ks + {0,1} (k = 2q4, 2q4+1) and + {2,3} (k = 2q4+8, +9).
+template <int D, bool FP8>
+__device__ __forceinline__ void load_q(const DecodeArgs& a, int b, int kvh, int lane,
+                                       uint32_t (&qa)[D / 16][2]) {
+  const int G = a.group, r = lane >> 2, q4 = lane & 3;
+  const __nv_bfloat16* qrow = static_cast<const __nv_bfloat16*>(a.q) +
+                              (static_cast<long long>(b) * a.num_heads + kvh * G + min(r, G - 1)) * D;
+#pragma unroll
+  for (int ks = 0; ks < D / 16; ++ks) {
+    if (r < G) {
+      if constexpr (!FP8) {
+        qa[ks][0] = *reinterpret_cast<const uint32_t*>(qrow + ks * 16 + 2 * q4);
+        qa[ks][1] = *reinterpret_cast<const uint32_t*>(qrow + ks * 16 + 8 + 2 * q4);
+      } else {
+        const uint2 raw4 = *reinterpret_cast<const uint2*>(qrow + 32 * q4 + 4 * ks);
+        const __nv_bfloat162 lo = *reinterpret_cast<const __nv_bfloat162*>(&raw4.x);
+        const __nv_bfloat162 hi = *reinterpret_cast<const __nv_bfloat162*>(&raw4.y);
+        qa[ks][0] = pack_f16x2(__low2float(lo), __high2float(lo));
+        qa[ks][1] = pack_f16x2(__low2float(hi), __high2float(hi));
+      }
+    } else {
+      qa[ks][0] = 0u;
+      qa[ks][1] = 0u;
+    }
+  }
+}
+
+// One physical block (tokens tok0 .. tok0+BS-1, of which those < L count)
+// staged in shared memory at kt (K) / vt (V), FP8 scales at ksc / vsc:
+// fold it into the warp's online-softmax state (m_run, l_run for head r of
+// lane group r; acc = O^T fragments for heads 2q4, 2q4+1).
+template <int D, int BS, bool FP8>
+__device__ __forceinline__ void attend_block(uint32_t kt, uint32_t vt, const uint8_t* base_ptr,
+                                             uint32_t base, const float* ksc, const float* vsc,
+                                             int tok0, int L, const uint32_t (&qa)[D / 16][2],
+                                             float (&acc)[D / 16][4], float& m_run, float& l_run,
+                                             float sl2, int lane) {
+  const int r = lane >> 2, q4 = lane & 3;
+#pragma unroll
+  for (int hf = 0; hf < BS / 16; ++hf) {
+    const int htok = tok0 + hf * 16;
+    if (htok >= L) break;
+    const bool partial = htok + 16 > L;
+    // ---- S = Q K^T for 16 tokens (two n-tiles of 8)
+    float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    if constexpr (!FP8) {
+      const int mi = lane >> 3;
+      const int row = hf * 16 + (mi >> 1) * 8 + (lane & 7);
+#pragma unroll
+      for (int ks = 0; ks < D / 16; ++ks) {
+        uint32_t b00, b01, b10, b11;
+        ldmatrix_x4(swz<BS>(kt, row, 2 * ks + (mi & 1)), b00, b01, b10, b11);
+        mma_bf16(sc[0], qa[ks][0], 0u, qa[ks][1], 0u, b00, b01);
+        mma_bf16(sc[1], qa[ks][0], 0u, qa[ks][1], 0u, b10, b11);
+      }
+    } else {
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        const int row = hf * 16 + nt * 8 + r;
+        uint32_t w[8];
+        const uint4 c0 =
+            *reinterpret_cast<const uint4*>(base_ptr + (swz<BS>(kt, row, 2 * q4) - base));
+        const uint4 c1 =
+            *reinterpret_cast<const uint4*>(base_ptr + (swz<BS>(kt, row, 2 * q4 + 1) - base));
+        w[0] = c0.x; w[1] = c0.y; w[2] = c0.z; w[3] = c0.w;
+        w[4] = c1.x; w[5] = c1.y; w[6] = c1.z; w[7] = c1.w;
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks)
+          mma_f16(sc[nt], qa[ks][0], 0u, qa[ks][1], 0u, e4m3x2_to_f16x2(w[ks] & 0xffffu),
+                  e4m3x2_to_f16x2(w[ks] >> 16));
+      }
+    }
+    // ---- online softmax for head r over tokens htok + nt*8 + 2q4 + {0,1}
+    float x[4];
+    if constexpr (!FP8) {
+      x[0] = sc[0][0] * sl2;
+      x[1] = sc[0][1] * sl2;
+      x[2] = sc[1][0] * sl2;
+      x[3] = sc[1][1] * sl2;
+    } else {
+      const float2 k0 = *reinterpret_cast<const float2*>(ksc + hf * 16 + 2 * q4);
+      const float2 k1 = *reinterpret_cast<const float2*>(ksc + hf * 16 + 8 + 2 * q4);
+      x[0] = sc[0][0] * (k0.x * sl2);
+      x[1] = sc[0][1] * (k0.y * sl2);
+      x[2] = sc[1][0] * (k1.x * sl2);
+      x[3] = sc[1][1] * (k1.y * sl2);
+    }
+    bool valid[4] = {true, true, true, true};
+    if (partial) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        valid[j] = htok + (j >> 1) * 8 + 2 * q4 + (j & 1) < L;
+        if (!valid[j]) x[j] = -INFINITY;
+      }
+    }
+    float mx = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
+    mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 2));
+    const float m_new = fmaxf(m_run, mx);
+    const float alpha = fast_exp2(m_run - m_new);
+    float pr[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) pr[j] = fast_exp2(x[j] - m_new);
+    l_run = l_run * alpha + ((pr[0] + pr[1]) + (pr[2] + pr[3]));
+    m_run = m_new;
+    // accumulator columns are heads 2q4 and 2q4+1: fetch their factors
+    const float al0 = __shfl_sync(kFull, alpha, 8 * q4);
+    const float al1 = __shfl_sync(kFull, alpha, 8 * q4 + 4);
+#pragma unroll
+    for (int mt = 0; mt < D / 16; ++mt) {
+      acc[mt][0] *= al0;
+      acc[mt][1] *= al1;
+      acc[mt][2] *= al0;
+      acc[mt][3] *= al1;
+    }
+    // token-validity masks for the V^T fragments (lo half = token 2q4(+8))
+    uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;
+    if (partial) {
+      mlo = (valid[0] ? 0x0000ffffu : 0u) | (valid[1] ? 0xffff0000u : 0u);
+      mhi = (valid[2] ? 0x0000ffffu : 0u) | (valid[3] ? 0xffff0000u : 0u);
+    }
+    // ---- O^T += V^T P^T
+    if constexpr (!FP8) {
+      const uint32_t pb0 = pack_bf16x2(pr[0], pr[1]);
+      const uint32_t pb1 = pack_bf16x2(pr[2], pr[3]);
+      const int mi = lane >> 3;
+      const int row = hf * 16 + (mi >> 1) * 8 + (lane & 7);
+#pragma unroll
+      for (int mt = 0; mt < D / 16; ++mt) {
+        uint32_t a0, a1, a2, a3;
+        ldmatrix_x4_trans(swz<BS>(vt, row, 2 * mt + (mi & 1)), a0, a1, a2, a3);
+        mma_bf16(acc[mt], a0 & mlo, a1 & mlo, a2 & mhi, a3 & mhi, pb0, pb1);
+      }
+    } else {
+      const float2 v0 = *reinterpret_cast<const float2*>(vsc + hf * 16 + 2 * q4);
+      const float2 v1 = *reinterpret_cast<const float2*>(vsc + hf * 16 + 8 + 2 * q4);
+      const uint32_t pb0 = pack_f16x2(valid[0] ? pr[0] * v0.x : 0.f, valid[1] ? pr[1] * v0.y : 0.f);
+      const uint32_t pb1 = pack_f16x2(valid[2] ? pr[2] * v1.x : 0.f, valid[3] ? pr[3] * v1.y : 0.f);
+      // lane (r, q4) reads 16-byte chunk r of token rows 2q4, 2q4+1, 2q4+8, 2q4+9:
+      // word w gives dims 16r + 4w + {0..3}; output row mapping in store_warp_state.
+      const int t0 = hf * 16 + 2 * q4;
+      const uint4 W0 = *reinterpret_cast<const uint4*>(base_ptr + (swz<BS>(vt, t0, r) - base));
+      const uint4 W1 = *reinterpret_cast<const uint4*>(base_ptr + (swz<BS>(vt, t0 + 1, r) - base));
+      const uint4 W8 = *reinterpret_cast<const uint4*>(base_ptr + (swz<BS>(vt, t0 + 8, r) - base));
+      const uint4 W9 = *reinterpret_cast<const uint4*>(base_ptr + (swz<BS>(vt, t0 + 9, r) - base));
+      const uint32_t w0[4] = {W0.x, W0.y, W0.z, W0.w};
+      const uint32_t w1[4] = {W1.x, W1.y, W1.z, W1.w};
+      const uint32_t w8[4] = {W8.x, W8.y, W8.z, W8.w};
+      const uint32_t w9[4] = {W9.x, W9.y, W9.z, W9.w};
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+#pragma unroll
+        for (int o = 0; o < 2; ++o) {
+          const uint32_t sel = o ? 0x7362u : 0x5140u;
+          const uint32_t p01 = prmt(w0[w], w1[w], sel);
+          const uint32_t p89 = prmt(w8[w], w9[w], sel);
+          const uint32_t a0 = e4m3x2_to_f16x2(p01 & 0xffffu) & mlo;
+          const uint32_t a1 = e4m3x2_to_f16x2(p01 >> 16) & mlo;
+          const uint32_t a2 = e4m3x2_to_f16x2(p89 & 0xffffu) & mhi;
+          const uint32_t a3 = e4m3x2_to_f16x2(p89 >> 16) & mhi;
+          mma_f16(acc[2 * w + o], a0, a1, a2, a3, pb0, pb1);
+        }
+      }
+    }
+  }
+}
+
+// Write a warp's (max, sum, O) for its 8 head rows into the merge buffer.
+template <int D, int NW, bool FP8>
+__device__ __forceinline__ void store_warp_state(float* mo, int warp, int lane, float m_run,
+                                                 float l_run, const float (&acc)[D / 16][4]) {
+  constexpr int S = D + 4;
+  const int r = lane >> 2, q4 = lane & 3;
+  float l_tot = l_run + __shfl_xor_sync(kFull, l_run, 1);
+  l_tot += __shfl_xor_sync(kFull, l_tot, 2);
+  float* mm = mo + NW * 8 * S;  // [NW][8] max
+  float* ml = mm + NW * 8;      // [NW][8] sum
+  if (q4 == 0) {
+    mm[warp * 8 + r] = m_run;
+    ml[warp * 8 + r] = l_tot;
+  }
+#pragma unroll
+  for (int mt = 0; mt < D / 16; ++mt) {
+    int d0, d1;
+    if constexpr (!FP8) {
+      d0 = mt * 16 + r;
+      d1 = d0 + 8;
+    } else {
+      d0 = 16 * r + 4 * (mt >> 1) + 2 * (mt & 1);
+      d1 = d0 + 1;
+    }
+    float* row0 = mo + (warp * 8 + 2 * q4) * S;
+    float* row1 = row0 + S;
+    row0[d0] = acc[mt][0];
+    row1[d0] = acc[mt][1];
+    row0[d1] = acc[mt][2];
+    row1[d1] = acc[mt][3];
+  }
+}
+
+// Merge the NW warp states of kv head `kvh` of sequence b and write either the
+// bf16 output (final) or one fp32 partial (O unnormalised, (max, sum)) to
+// partial slot `slot`.
+template <int D, int NW>
+__device__ __forceinline__ void merge_warps_and_write(const float* mo, const DecodeArgs& a, int b,
+                                                      int kvh, bool final_out, long long slot) {
+  constexpr int S = D + 4;
+  const float* mm = mo + NW * 8 * S;
+  const float* ml = mm + NW * 8;
+  const int G = a.group;
+  for (int e = threadIdx.x; e < G * D; e += NW * 32) {
+    const int g = e / D, d = e - g * D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) M = fmaxf(M, mm[w * 8 + g]);
+    float o = 0.f, l = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < NW; ++w) {
+        const float f = fast_exp2(mm[w * 8 + g] - M);
+        o += f * mo[(w * 8 + g) * S + d];
+        l += f * ml[w * 8 + g];
+      }
+    }
+    if (final_out) {
+      const long long bh = static_cast<long long>(b) * a.num_heads + kvh * G + g;
+      static_cast<__nv_bfloat16*>(a.out)[bh * D + d] = __float2bfloat16_rn(l > 0.f ? o / l : 0.f);
+    } else {
+      a.part_o[(slot * 8 + g) * D + d] = o;
+      if (d == 0) {
+        a.part_ml[(slot * 8 + g) * 2 + 0] = M;
+        a.part_ml[(slot * 8 + g) * 2 + 1] = l;
+      }
+    }
+  }
+}
+
+// ============================================================ persistent path
+// Flattened work: segment (b, kvh) in b-major order holds nblk(b) blocks; the
+// global index of its first block is prefix[b] * Hkv + kvh * nblk(b). CTA c of
+// P owns [c*N/P, (c+1)*N/P) with N = prefix[B] * Hkv.
+struct Piece {
+  int b, kvh, lo, hi;  // segment and its block range owned by this CTA
+  int nblk;            // blocks of the segment
+  long long g;         // global index of block `lo`
+  bool valid;
+};
+
+__device__ __forceinline__ void piece_first(Piece& p, const int* prefix, int B, int Hkv,
+                                            long long r0, long long r1) {
+  p.valid = r0 < r1;
+  if (!p.valid) return;
+  // last b with prefix[b] * Hkv <= r0 (it has nblk > 0 since r0 < prefix[B] * Hkv)
+  int lo = 0, hi = B;  // invariant: prefix[lo]*Hkv <= r0 < prefix[hi]*Hkv
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (static_cast<long long>(prefix[mid]) * Hkv <= r0) lo = mid; else hi = mid;
+  }
+  p.b = lo;
+  p.nblk = prefix[lo + 1] - prefix[lo];
+  const long long off = r0 - static_cast<long long>(prefix[lo]) * Hkv;
+  p.kvh = static_cast<int>(off / p.nblk);
+  p.lo = static_cast<int>(off % p.nblk);
+  p.hi = static_cast<int>(min(static_cast<long long>(p.nblk), p.lo + (r1 - r0)));
+  p.g = r0;
+}
+
+__device__ __forceinline__ void piece_next(Piece& p, const int* prefix, int B, int Hkv,
+                                           long long r1) {
+  p.g += p.hi - p.lo;
+  if (p.g >= r1) {
+    p.valid = false;
+    return;
+  }
+  if (++p.kvh == Hkv) {
+    p.kvh = 0;
+    do {
+      ++p.b;
+    } while (p.b < B && prefix[p.b + 1] == prefix[p.b]);
+  }
+  p.nblk = prefix[p.b + 1] - prefix[p.b];
+  p.lo = 0;
+  p.hi = static_cast<int>(min(static_cast<long long>(p.nblk), r1 - p.g));
+}
+
+template <int D, int BS, int NW, int ST, bool FP8>
+struct PCfg {
+  using C = Cfg<D, BS, NW, ST, FP8>;
+  static constexpr int kRings = C::kTiles;
+  static constexpr int kScaleOff = kRings;
+  static constexpr int kMergeOff = kScaleOff + C::kScaleBytes;
+  static constexpr int kPrefixOff = kMergeOff + 2 * C::kMerge;
+  static int smem_bytes(int batch) { return 1024 + kPrefixOff + (batch + 1) * 4; }
+};
+
+template <int D, int BS, int NW, int ST, bool FP8>
+__global__ void __launch_bounds__(NW * 32)
+    decode_persistent_kernel(const __grid_constant__ CUtensorMap kmap,
+                             const __grid_constant__ CUtensorMap vmap, const DecodeArgs a) {
+  using C = Cfg<D, BS, NW, ST, FP8>;
+  using PC = PCfg<D, BS, NW, ST, FP8>;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t bars[NW * ST];
+  __shared__ int warp_sums[NW];
+
+  const uint32_t raw = smem_addr(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* const base_ptr = smem_raw + (base - raw);
+  const uint32_t scale_base = base + PC::kScaleOff;
+  const float* const scale_ptr = reinterpret_cast<const float*>(base_ptr + PC::kScaleOff);
+  float* const merge_buf = reinterpret_cast<float*>(base_ptr + PC::kMergeOff);
+  int* const prefix = reinterpret_cast<int*>(base_ptr + PC::kPrefixOff);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int B = a.batch, Hkv = a.num_kv_heads;
+  const int c = blockIdx.x, P = gridDim.x;
+
+  // ---- blocks per sequence and their exclusive prefix sum (whole CTA)
+  int carry = 0;
+  for (int base_i = 0; base_i < B; base_i += NW * 32) {
+    const int i = base_i + threadIdx.x;
+    int v = 0;
+    if (i < B) v = (min(max(a.context_lens[i], 0), a.len_cap) + BS - 1) / BS;
+    int incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(kFull, incl, o);
+      if (lane >= o) incl += t;
+    }
+    if (lane == 31) warp_sums[warp] = incl;
+    __syncthreads();
+    int wbase = 0, total = 0;
+    for (int w = 0; w < NW; ++w) {
+      if (w < warp) wbase += warp_sums[w];
+      total += warp_sums[w];
+    }
+    if (i < B) prefix[i] = carry + wbase + incl - v;
+    carry += total;
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) prefix[B] = carry;
+  __syncthreads();
+  if (c == 0)
+    for (int i = threadIdx.x; i <= B; i += NW * 32) a.prefix_out[i] = prefix[i];
+
+  const long long N = static_cast<long long>(prefix[B]) * Hkv;
+  const long long r0 = c * N / P, r1 = (c + 1) * N / P;
+  if (r0 >= r1) return;  // whole CTA: no work
+
+  const uint32_t bar0 = smem_addr(&bars[warp * ST]);
+  const uint32_t stage0 = base + warp * ST * C::kStage;
+  if (lane == 0) {
+    for (int s = 0; s < ST; ++s) mbar_init(bar0 + 8 * s, 1);
+    fence_barrier_init();
+    fence_proxy_async_smem();
+  }
+  __syncwarp();
+
+  // ---- producer: this warp's blocks in order, across pieces
+  Piece pp;
+  piece_first(pp, prefix, B, Hkv, r0, r1);
+  int pp_next = pp.lo + warp;
+  bool pend = false;
+  int pend_kvh = 0, pend_phys = 0;
+  auto fetch_next = [&]() {  // find the next block of this warp, start loading its id
+    pend = false;
+    while (pp.valid) {
+      if (pp_next < pp.hi) {
+        pend = true;
+        pend_kvh = pp.kvh;
+        pend_phys = a.block_tables[static_cast<long long>(pp.b) * a.max_blocks + pp_next];
+        pp_next += NW;
+        return;
+      }
+      piece_next(pp, prefix, B, Hkv, r1);
+      pp_next = pp.lo + warp;
+    }
+  };
+  int issued = 0;
+  auto issue_pending = [&]() {
+    if (!pend) return;
+    int phys = pend_phys;
+    if (phys < 0 || phys >= a.num_blocks) {
+      if (lane == 0) report_error(a.err, PA_DEVERR_BLOCK_RANGE);
+      phys = 0;  // stay inside the pool; the result is flagged as invalid
+    }
+    if (lane == 0) {
+      const int s = issued % ST;
+      const uint32_t bar = bar0 + 8 * s;
+      const uint32_t kt = stage0 + s * C::kStage;
+      mbar_arrive_expect_tx(bar, C::kTx);
+#pragma unroll
+      for (int j = 0; j < C::kNSub; ++j) {
+        tma_load_3d(kt + j * C::kSubBytes, &kmap, bar, j * (kSwizzleBytes / C::kElem), pend_kvh,
+                    phys * BS);
+        tma_load_3d(kt + C::kTile + j * C::kSubBytes, &vmap, bar,
+                    j * (kSwizzleBytes / C::kElem), pend_kvh, phys * BS);
+      }
+      if constexpr (FP8) {
+        const long long off = (static_cast<long long>(phys) * Hkv + pend_kvh) * BS;
+        const uint32_t sc = scale_base + ((warp * ST + s) * 2) * BS * 4;
+        bulk_load(sc, a.k_scale + off, BS * 4, bar);
+        bulk_load(sc + BS * 4, a.v_scale + off, BS * 4, bar);
+      }
+    }
+    ++issued;
+    fetch_next();
+  };
+  fetch_next();
+  for (int s = 0; s < ST; ++s) issue_pending();
+
+  // ---- consumer: pieces in order; all warps meet at each piece end
+  Piece cp;
+  piece_first(cp, prefix, B, Hkv, r0, r1);
+  const float sl2 = a.scale_log2;
+  int consumed = 0, piece_idx = 0;
+  bool ok = true;
+  while (cp.valid) {
+    uint32_t qa[D / 16][2];
+    load_q<D, FP8>(a, cp.b, cp.kvh, lane, qa);
+    const int L = min(max(a.context_lens[cp.b], 0), a.len_cap);
+    float acc[D / 16][4];
+#pragma unroll
+    for (int mt = 0; mt < D / 16; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
+    float m_run = -INFINITY, l_run = 0.f;
+    for (int blk = cp.lo + warp; ok && blk < cp.hi; blk += NW) {
+      const int s = consumed % ST;
+      const bool got = mbar_wait(bar0 + 8 * s, (consumed / ST) & 1);
+      if (!__all_sync(kFull, got)) {
+        ok = false;
+        if (lane == 0) report_error(a.err, PA_DEVERR_WAIT_TIMEOUT);
+        break;
+      }
+      const uint32_t kt = stage0 + s * C::kStage;
+      const float* ksc = scale_ptr + ((warp * ST + s) * 2) * BS;
+      attend_block<D, BS, FP8>(kt, kt + C::kTile, base_ptr, base, ksc, ksc + BS, blk * BS, L, qa,
+                               acc, m_run, l_run, sl2, lane);
+      ++consumed;
+      __syncwarp();
+      issue_pending();
+    }
+    float* mo = merge_buf + (piece_idx & 1) * (C::kMerge / 4);
+    store_warp_state<D, NW, FP8>(mo, warp, lane, m_run, l_run, acc);
+    // all warps of the CTA: every one walks the same pieces
+    asm volatile("bar.sync 1, %0;" ::"n"(NW * 32) : "memory");
+    const bool whole = cp.lo == 0 && cp.hi == cp.nblk;
+    const long long slot = 2LL * c + (cp.lo == 0 ? 1 : 0);
+    if (ok) merge_warps_and_write<D, NW>(mo, a, cp.b, cp.kvh, whole, slot);
+    ++piece_idx;
+    piece_next(cp, prefix, B, Hkv, r1);
+  }
+  if (!ok) {
+    // give copies still in flight a bounded chance to land before exit
+    for (int i = consumed; i < issued; ++i) (void)mbar_wait(bar0 + 8 * (i % ST), (i / ST) & 1);
+  }
+}
+
+// Finish segments that straddle CTAs: for segment (b, kvh) over global blocks
+// [s0, s1), CTA owner(s0) left its piece in slot 2*owner(s0)+1 and every
+// later CTA up to owner(s1-1) (with a non-empty range) in slot 2*c. Merge:
+// M = max m_j, l = sum l_j 2^(m_j - M), o = sum o_j 2^(m_j - M) / l (base-2
+// scores). Sequences with no keys get zero rows. One warp per (b, query head).
+template <int D>
+__global__ void __launch_bounds__(128) decode_persistent_merge_kernel(const DecodeArgs a, int P) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long gw = static_cast<long long>(blockIdx.x) * 4 + warp;
+  if (gw >= static_cast<long long>(a.batch) * a.num_heads) return;
+  const int b = static_cast<int>(gw / a.num_heads);
+  const int h = static_cast<int>(gw % a.num_heads);
+  const int G = a.group, kvh = h / G, g = h % G, Hkv = a.num_kv_heads;
+  const int* prefix = a.prefix_out;
+  const int nblk = prefix[b + 1] - prefix[b];
+  constexpr int V = D / 32;  // dims per lane
+  __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.out) + gw * D + lane * V;
+  if (nblk == 0) {
+#pragma unroll
+    for (int v = 0; v < V; v += 2)
+      *reinterpret_cast<__nv_bfloat162*>(dst + v) = __floats2bfloat162_rn(0.f, 0.f);
+    return;
+  }
+  const long long N = static_cast<long long>(prefix[a.batch]) * Hkv;
+  const long long s0 = static_cast<long long>(prefix[b]) * Hkv + static_cast<long long>(kvh) * nblk;
+  const long long s1 = s0 + nblk;
+  auto owner = [&](long long x) { return static_cast<int>(((x + 1) * P - 1) / N); };
+  auto start = [&](int cc) { return cc * N / P; };
+  const int c0 = owner(s0), c1 = owner(s1 - 1);
+  if (c0 == c1) return;  // written by the CTA that held the whole segment
+  float M = -INFINITY;
+  for (int cc = c0; cc <= c1; ++cc) {
+    if (cc > c0 && start(cc) == start(cc + 1)) continue;  // empty range
+    const long long slot = cc == c0 ? 2LL * cc + 1 : 2LL * cc;
+    M = fmaxf(M, a.part_ml[(slot * 8 + g) * 2]);
+  }
+  float l = 0.f, acc[V];
+#pragma unroll
+  for (int v = 0; v < V; ++v) acc[v] = 0.f;
+  for (int cc = c0; cc <= c1; ++cc) {
+    if (cc > c0 && start(cc) == start(cc + 1)) continue;
+    const long long slot = cc == c0 ? 2LL * cc + 1 : 2LL * cc;
+    const float f = fast_exp2(a.part_ml[(slot * 8 + g) * 2] - M);
+    l += f * a.part_ml[(slot * 8 + g) * 2 + 1];
+    const float* src = a.part_o + (slot * 8 + g) * D + lane * V;
+#pragma unroll
+    for (int v = 0; v < V; ++v) acc[v] += f * src[v];
+  }
+  const float inv = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll
+  for (int v = 0; v < V; v += 2)
+    *reinterpret_cast<__nv_bfloat162*>(dst + v) = __floats2bfloat162_rn(acc[v] * inv, acc[v + 1] * inv);
+}
+
+// ============================================================ grid-split path
+// Grid (Hkv, B, S): CTA = (kv head, sequence, split of blocks_per_split
+// blocks). Used for batches too large for the persistent kernel's prefix.
 template <int D, int BS, int NW, int ST, bool FP8>
 __global__ void __launch_bounds__(NW * 32)
     decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
@@ -80,13 +603,12 @@ __global__ void __launch_bounds__(NW * 32)
   const uint32_t raw = smem_addr(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* const base_ptr = smem_raw + (base - raw);
-  const uint32_t scale_base = base + C::kRegion;
-  const float* const scale_ptr = reinterpret_cast<const float*>(base_ptr + C::kRegion);
+  const uint32_t scale_base = base + C::kTiles;
+  const float* const scale_ptr = reinterpret_cast<const float*>(base_ptr + C::kTiles);
+  float* const merge_buf = reinterpret_cast<float*>(base_ptr + C::kTiles + C::kScaleBytes);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int r = lane >> 2, q4 = lane & 3;  // MMA fragment row / quad position
   const int kvh = blockIdx.x, b = blockIdx.y, split = blockIdx.z;
-  const int G = a.group;
 
   const int L = min(max(a.context_lens[b], 0), a.len_cap);
   const int nblk = (L + BS - 1) / BS;
@@ -103,7 +625,7 @@ __global__ void __launch_bounds__(NW * 32)
     my_phys = a.block_tables[static_cast<long long>(b) * a.max_blocks + blk0 + warp + lane * NW];
     if (my_phys < 0 || my_phys >= a.num_blocks) {
       report_error(a.err, PA_DEVERR_BLOCK_RANGE);
-      my_phys = 0;  // stay inside the pool; the result is flagged as invalid
+      my_phys = 0;
     }
   }
 
@@ -142,41 +664,12 @@ __global__ void __launch_bounds__(NW * 32)
   const int n_pre = min(ST, n_my);
   for (int i = 0; i < n_pre; ++i) issue(i);
 
-  // Q fragments (A operand of S = Q K^T): row r = head of the group.
-  // bf16: k index of step ks = head_dim ks*16 + {2q4, 2q4+1, 2q4+8, 2q4+9}.
-  // FP8 (f16 MMA): the head_dim order inside a step is permuted to match how
-  // the K codes are read (lane quad q4 owns dims [32 q4, 32 q4 + 32)): step ks
-  // uses dims 32 q4 + 4 ks + {0,1} (k = 2q4, 2q4+1) and + {2,3} (k = 2q4+8, +9).
   uint32_t qa[D / 16][2];
-  {
-    const __nv_bfloat16* qrow =
-        static_cast<const __nv_bfloat16*>(a.q) +
-        (static_cast<long long>(b) * a.num_heads + kvh * G + min(r, G - 1)) * D;
-#pragma unroll
-    for (int ks = 0; ks < D / 16; ++ks) {
-      if (r < G) {
-        if constexpr (!FP8) {
-          qa[ks][0] = *reinterpret_cast<const uint32_t*>(qrow + ks * 16 + 2 * q4);
-          qa[ks][1] = *reinterpret_cast<const uint32_t*>(qrow + ks * 16 + 8 + 2 * q4);
-        } else {
-          const uint2 raw4 = *reinterpret_cast<const uint2*>(qrow + 32 * q4 + 4 * ks);
-          const __nv_bfloat162 lo = *reinterpret_cast<const __nv_bfloat162*>(&raw4.x);
-          const __nv_bfloat162 hi = *reinterpret_cast<const __nv_bfloat162*>(&raw4.y);
-          qa[ks][0] = pack_f16x2(__low2float(lo), __high2float(lo));
-          qa[ks][1] = pack_f16x2(__low2float(hi), __high2float(hi));
-        }
-      } else {
-        qa[ks][0] = 0u;
-        qa[ks][1] = 0u;
-      }
-    }
-  }
-
+  load_q<D, FP8>(a, b, kvh, lane, qa);
   float acc[D / 16][4];
 #pragma unroll
   for (int mt = 0; mt < D / 16; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
   float m_run = -INFINITY, l_run = 0.f;
-  const float sl2 = a.scale_log2;
 
   bool ok = true;
   int consumed = 0;
@@ -189,268 +682,72 @@ __global__ void __launch_bounds__(NW * 32)
     }
     consumed = i + 1;
     const uint32_t kt = stage0 + s * C::kStage;
-    const uint32_t vt = kt + C::kTile;
-    const int tok0 = (blk0 + warp + i * NW) * BS;
     const float* ksc = scale_ptr + ((warp * ST + s) * 2) * BS;
-    const float* vsc = ksc + BS;
-
-#pragma unroll
-    for (int hf = 0; hf < BS / 16; ++hf) {
-      const int htok = tok0 + hf * 16;
-      if (htok >= L) break;
-      const bool partial = htok + 16 > L;
-      // ---- S = Q K^T for 16 tokens (two n-tiles of 8)
-      float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-      if constexpr (!FP8) {
-        const int mi = lane >> 3;
-        const int row = hf * 16 + (mi >> 1) * 8 + (lane & 7);
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          uint32_t b00, b01, b10, b11;
-          ldmatrix_x4(swz<BS>(kt, row, 2 * ks + (mi & 1)), b00, b01, b10, b11);
-          mma_bf16(sc[0], qa[ks][0], 0u, qa[ks][1], 0u, b00, b01);
-          mma_bf16(sc[1], qa[ks][0], 0u, qa[ks][1], 0u, b10, b11);
-        }
-      } else {
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-          const int row = hf * 16 + nt * 8 + r;
-          uint32_t w[8];
-          const uint4 c0 = *reinterpret_cast<const uint4*>(
-              base_ptr + (swz<BS>(kt, row, 2 * q4) - base));
-          const uint4 c1 = *reinterpret_cast<const uint4*>(
-              base_ptr + (swz<BS>(kt, row, 2 * q4 + 1) - base));
-          w[0] = c0.x; w[1] = c0.y; w[2] = c0.z; w[3] = c0.w;
-          w[4] = c1.x; w[5] = c1.y; w[6] = c1.z; w[7] = c1.w;
-#pragma unroll
-          for (int ks = 0; ks < D / 16; ++ks)
-            mma_f16(sc[nt], qa[ks][0], 0u, qa[ks][1], 0u, e4m3x2_to_f16x2(w[ks] & 0xffffu),
-                    e4m3x2_to_f16x2(w[ks] >> 16));
-        }
-      }
-      // ---- online softmax for head r over tokens htok + nt*8 + 2q4 + {0,1}
-      float x[4];
-      if constexpr (!FP8) {
-        x[0] = sc[0][0] * sl2;
-        x[1] = sc[0][1] * sl2;
-        x[2] = sc[1][0] * sl2;
-        x[3] = sc[1][1] * sl2;
-      } else {
-        const float2 k0 = *reinterpret_cast<const float2*>(ksc + hf * 16 + 2 * q4);
-        const float2 k1 = *reinterpret_cast<const float2*>(ksc + hf * 16 + 8 + 2 * q4);
-        x[0] = sc[0][0] * (k0.x * sl2);
-        x[1] = sc[0][1] * (k0.y * sl2);
-        x[2] = sc[1][0] * (k1.x * sl2);
-        x[3] = sc[1][1] * (k1.y * sl2);
-      }
-      bool valid[4] = {true, true, true, true};
-      if (partial) {
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          valid[j] = htok + (j >> 1) * 8 + 2 * q4 + (j & 1) < L;
-          if (!valid[j]) x[j] = -INFINITY;
-        }
-      }
-      float mx = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
-      mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 1));
-      mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 2));
-      const float m_new = fmaxf(m_run, mx);
-      const float alpha = fast_exp2(m_run - m_new);
-      float pr[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) pr[j] = fast_exp2(x[j] - m_new);
-      l_run = l_run * alpha + ((pr[0] + pr[1]) + (pr[2] + pr[3]));
-      m_run = m_new;
-      // accumulator columns are heads 2q4 and 2q4+1: fetch their factors
-      const float al0 = __shfl_sync(kFull, alpha, 8 * q4);
-      const float al1 = __shfl_sync(kFull, alpha, 8 * q4 + 4);
-#pragma unroll
-      for (int mt = 0; mt < D / 16; ++mt) {
-        acc[mt][0] *= al0;
-        acc[mt][1] *= al1;
-        acc[mt][2] *= al0;
-        acc[mt][3] *= al1;
-      }
-      // token-validity masks for the V^T fragments (lo half = token 2q4(+8))
-      uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;
-      if (partial) {
-        mlo = (valid[0] ? 0x0000ffffu : 0u) | (valid[1] ? 0xffff0000u : 0u);
-        mhi = (valid[2] ? 0x0000ffffu : 0u) | (valid[3] ? 0xffff0000u : 0u);
-      }
-      // ---- O^T += V^T P^T
-      if constexpr (!FP8) {
-        const uint32_t pb0 = pack_bf16x2(pr[0], pr[1]);
-        const uint32_t pb1 = pack_bf16x2(pr[2], pr[3]);
-        const int mi = lane >> 3;
-        const int row = hf * 16 + (mi >> 1) * 8 + (lane & 7);
-#pragma unroll
-        for (int mt = 0; mt < D / 16; ++mt) {
-          uint32_t a0, a1, a2, a3;
-          ldmatrix_x4_trans(swz<BS>(vt, row, 2 * mt + (mi & 1)), a0, a1, a2, a3);
-          mma_bf16(acc[mt], a0 & mlo, a1 & mlo, a2 & mhi, a3 & mhi, pb0, pb1);
-        }
-      } else {
-        const float2 v0 = *reinterpret_cast<const float2*>(vsc + hf * 16 + 2 * q4);
-        const float2 v1 = *reinterpret_cast<const float2*>(vsc + hf * 16 + 8 + 2 * q4);
-        const uint32_t pb0 = pack_f16x2(valid[0] ? pr[0] * v0.x : 0.f,
-                                        valid[1] ? pr[1] * v0.y : 0.f);
-        const uint32_t pb1 = pack_f16x2(valid[2] ? pr[2] * v1.x : 0.f,
-                                        valid[3] ? pr[3] * v1.y : 0.f);
-        // lane (r, q4) reads 16-byte chunk r of token rows 2q4, 2q4+1, 2q4+8, 2q4+9:
-        // word w gives dims 16r + 4w + {0..3}; output row mapping below.
-        const int t0 = hf * 16 + 2 * q4;
-        const uint4 W0 = *reinterpret_cast<const uint4*>(base_ptr + (swz<BS>(vt, t0, r) - base));
-        const uint4 W1 =
-            *reinterpret_cast<const uint4*>(base_ptr + (swz<BS>(vt, t0 + 1, r) - base));
-        const uint4 W8 =
-            *reinterpret_cast<const uint4*>(base_ptr + (swz<BS>(vt, t0 + 8, r) - base));
-        const uint4 W9 =
-            *reinterpret_cast<const uint4*>(base_ptr + (swz<BS>(vt, t0 + 9, r) - base));
-        const uint32_t w0[4] = {W0.x, W0.y, W0.z, W0.w};
-        const uint32_t w1[4] = {W1.x, W1.y, W1.z, W1.w};
-        const uint32_t w8[4] = {W8.x, W8.y, W8.z, W8.w};
-        const uint32_t w9[4] = {W9.x, W9.y, W9.z, W9.w};
-#pragma unroll
-        for (int w = 0; w < 4; ++w) {
-#pragma unroll
-          for (int o = 0; o < 2; ++o) {
-            const uint32_t sel = o ? 0x7362u : 0x5140u;
-            const uint32_t p01 = prmt(w0[w], w1[w], sel);
-            const uint32_t p89 = prmt(w8[w], w9[w], sel);
-            const uint32_t a0 = e4m3x2_to_f16x2(p01 & 0xffffu) & mlo;
-            const uint32_t a1 = e4m3x2_to_f16x2(p01 >> 16) & mlo;
-            const uint32_t a2 = e4m3x2_to_f16x2(p89 & 0xffffu) & mhi;
-            const uint32_t a3 = e4m3x2_to_f16x2(p89 >> 16) & mhi;
-            mma_f16(acc[2 * w + o], a0, a1, a2, a3, pb0, pb1);
-          }
-        }
-      }
-    }
+    attend_block<D, BS, FP8>(kt, kt + C::kTile, base_ptr, base, ksc, ksc + BS,
+                             (blk0 + warp + i * NW) * BS, L, qa, acc, m_run, l_run, a.scale_log2,
+                             lane);
     __syncwarp();
     if (i + ST < n_my) issue(i + ST);
   }
-
   if (!ok) {
-    // A copy never completed: report, then give the remaining in-flight copies
-    // a bounded chance to land before this CTA's shared memory is released.
     if (lane == 0) report_error(a.err, PA_DEVERR_WAIT_TIMEOUT);
     for (int i = consumed; i < min(n_my, consumed + ST); ++i)
       (void)mbar_wait(bar0 + 8 * (i % ST), (i / ST) & 1);
   }
-
-  // ---- merge the warps of this CTA
-  float l_tot = l_run + __shfl_xor_sync(kFull, l_run, 1);
-  l_tot += __shfl_xor_sync(kFull, l_tot, 2);
+  store_warp_state<D, NW, FP8>(merge_buf, warp, lane, m_run, l_run, acc);
   const bool any_fail = __syncthreads_or(!ok);
-  float* mo = reinterpret_cast<float*>(base_ptr);  // [NW][8][kMoStride]
-  float* mm = mo + NW * 8 * C::kMoStride;           // [NW][8]
-  float* ml = mm + NW * 8;                          // [NW][8]
-  if (q4 == 0) {
-    mm[warp * 8 + r] = m_run;
-    ml[warp * 8 + r] = l_tot;
-  }
-#pragma unroll
-  for (int mt = 0; mt < D / 16; ++mt) {
-    int d0, d1;
-    if constexpr (!FP8) {
-      d0 = mt * 16 + r;
-      d1 = d0 + 8;
-    } else {
-      d0 = 16 * r + 4 * (mt >> 1) + 2 * (mt & 1);
-      d1 = d0 + 1;
-    }
-    float* row0 = mo + (warp * 8 + 2 * q4) * C::kMoStride;
-    float* row1 = row0 + C::kMoStride;
-    row0[d0] = acc[mt][0];
-    row1[d0] = acc[mt][1];
-    row0[d1] = acc[mt][2];
-    row1[d1] = acc[mt][3];
-  }
-  __syncthreads();
   if (any_fail) return;
-
-  const int H = a.num_heads;
-  for (int e = threadIdx.x; e < G * D; e += NW * 32) {
-    const int g = e / D, d = e - g * D;
-    float M = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < NW; ++w) M = fmaxf(M, mm[w * 8 + g]);
-    float o = 0.f, l = 0.f;
-    if (M != -INFINITY) {
-#pragma unroll
-      for (int w = 0; w < NW; ++w) {
-        const float f = fast_exp2(mm[w * 8 + g] - M);
-        o += f * mo[(w * 8 + g) * C::kMoStride + d];
-        l += f * ml[w * 8 + g];
-      }
-    }
-    const long long bh = static_cast<long long>(b) * H + kvh * G + g;
-    if (nsplit_seq <= 1) {
-      static_cast<__nv_bfloat16*>(a.out)[bh * D + d] = __float2bfloat16_rn(l > 0.f ? o / l : 0.f);
-    } else {
-      a.part_o[(bh * a.num_splits + split) * D + d] = o;
-      if (d == 0) {
-        a.part_ml[(bh * a.num_splits + split) * 2 + 0] = M;
-        a.part_ml[(bh * a.num_splits + split) * 2 + 1] = l;
-      }
-    }
-  }
+  // partial slot of (b, kvh, split): the merge kernel below reads these
+  const long long slot = (static_cast<long long>(b) * a.num_kv_heads + kvh) * a.num_splits + split;
+  merge_warps_and_write<D, NW>(merge_buf, a, b, kvh, nsplit_seq <= 1, slot);
 }
 
-// Merge the per-split partials of sequences that needed more than one split:
-// M = max_j m_j, l = sum_j l_j 2^(m_j - M), o = sum_j o_j 2^(m_j - M) / l
-// (scores are kept in log2 units). One warp per (sequence, query head).
+// Merge the splits of sequences that needed more than one (grid-split path).
+// One warp per (sequence, query head).
 template <int D, int BS>
-__global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs a) {
+__global__ void __launch_bounds__(128) decode_split_merge_kernel(const DecodeArgs a) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const long long gw = static_cast<long long>(blockIdx.x) * 4 + warp;
   if (gw >= static_cast<long long>(a.batch) * a.num_heads) return;
   const int b = static_cast<int>(gw / a.num_heads);
+  const int h = static_cast<int>(gw % a.num_heads);
+  const int kvh = h / a.group, g = h % a.group;
   const int L = min(max(a.context_lens[b], 0), a.len_cap);
   const int nblk = (L + BS - 1) / BS;
   const int ns = (nblk + a.blocks_per_split - 1) / a.blocks_per_split;
   if (ns <= 1) return;
-  const float* ml = a.part_ml + gw * a.num_splits * 2;
-  const float* po = a.part_o + gw * a.num_splits * D;
+  const long long slot0 = (static_cast<long long>(b) * a.num_kv_heads + kvh) * a.num_splits;
   float M = -INFINITY;
-  for (int j = lane; j < ns; j += 32) M = fmaxf(M, ml[2 * j]);
+  for (int j = lane; j < ns; j += 32) M = fmaxf(M, a.part_ml[((slot0 + j) * 8 + g) * 2]);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
   float l = 0.f;
-  for (int j = lane; j < ns; j += 32) l += ml[2 * j + 1] * fast_exp2(ml[2 * j] - M);
+  for (int j = lane; j < ns; j += 32)
+    l += a.part_ml[((slot0 + j) * 8 + g) * 2 + 1] * fast_exp2(a.part_ml[((slot0 + j) * 8 + g) * 2] - M);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(kFull, l, o);
-  constexpr int V = D / 32;  // dims per lane
+  constexpr int V = D / 32;
   float acc[V];
 #pragma unroll
   for (int v = 0; v < V; ++v) acc[v] = 0.f;
   for (int j = 0; j < ns; ++j) {
-    const float f = fast_exp2(ml[2 * j] - M);
-    const float* src = po + static_cast<long long>(j) * D + lane * V;
-    if constexpr (V == 4) {
-      const float4 x = *reinterpret_cast<const float4*>(src);
-      acc[0] += f * x.x;
-      acc[1] += f * x.y;
-      acc[2] += f * x.z;
-      acc[3] += f * x.w;
-    } else {
-      const float2 x = *reinterpret_cast<const float2*>(src);
-      acc[0] += f * x.x;
-      acc[1] += f * x.y;
-    }
+    const float f = fast_exp2(a.part_ml[((slot0 + j) * 8 + g) * 2] - M);
+    const float* src = a.part_o + ((slot0 + j) * 8 + g) * D + lane * V;
+#pragma unroll
+    for (int v = 0; v < V; ++v) acc[v] += f * src[v];
   }
   const float inv = l > 0.f ? 1.f / l : 0.f;
   __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.out) + gw * D + lane * V;
 #pragma unroll
   for (int v = 0; v < V; v += 2)
-    *reinterpret_cast<__nv_bfloat162*>(dst + v) =
-        __floats2bfloat162_rn(acc[v] * inv, acc[v + 1] * inv);
+    *reinterpret_cast<__nv_bfloat162*>(dst + v) = __floats2bfloat162_rn(acc[v] * inv, acc[v + 1] * inv);
 }
 
+// ============================================================ host side
 constexpr int kWarps = 4;
-// Shared-memory budget of one CTA's stage rings: 96 KB lets two CTAs share an
-// SM (each warp keeps kStageBudget / (kWarps * stage) blocks in flight).
-constexpr int kStageBudget = 96 * 1024;
+// Shared-memory budget of one CTA's stage rings: 64 KB lets two CTAs share an
+// SM next to the merge buffers and the prefix sums.
+constexpr int kStageBudget = 64 * 1024;
 
 constexpr int stages_for(int stage_bytes) {
   return kStageBudget / (kWarps * stage_bytes) < 2 ? 2
@@ -459,24 +756,50 @@ constexpr int stages_for(int stage_bytes) {
 }
 
 template <int D, int BS, bool FP8>
-cudaError_t launch_t(const DecodeArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
-                     cudaStream_t stream) {
-  constexpr int kStages = stages_for(Cfg<D, BS, kWarps, 2, FP8>::kStage);
+struct Inst {
+  static constexpr int kStages = stages_for(Cfg<D, BS, kWarps, 2, FP8>::kStage);
   using C = Cfg<D, BS, kWarps, kStages, FP8>;
-  static_assert(C::kSmem <= 227 * 1024, "shared memory over the per-CTA limit");
-  auto* kern = decode_split_kernel<D, BS, kWarps, kStages, FP8>;
-  // The attribute is per device; setting it each call is cheap and avoids
-  // per-device bookkeeping.
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
-  if (e != cudaSuccess) return e;
-  dim3 grid(a.num_kv_heads, a.batch, a.num_splits);
-  kern<<<grid, kWarps * 32, C::kSmem, stream>>>(kmap, vmap, a);
-  e = cudaGetLastError();
-  if (e != cudaSuccess || a.num_splits <= 1) return e;
-  const long long rows = static_cast<long long>(a.batch) * a.num_heads;
-  decode_merge_kernel<D, BS><<<static_cast<unsigned>((rows + 3) / 4), 128, 0, stream>>>(a);
-  return cudaGetLastError();
-}
+  using PC = PCfg<D, BS, kWarps, kStages, FP8>;
+  static constexpr int kSplitSmem = 1024 + C::kTiles + C::kScaleBytes + C::kMerge;
+  static_assert(kSplitSmem <= 227 * 1024, "shared memory over the per-CTA limit");
+  static_assert(PC::kPrefixOff + 1024 + (kMaxPersistentBatch + 1) * 4 <= 227 * 1024,
+                "shared memory over the per-CTA limit");
+
+  static int ctas_per_sm(int batch) {
+    auto* k = decode_persistent_kernel<D, BS, kWarps, kStages, FP8>;
+    int n = 0;
+    const int smem = PC::smem_bytes(batch);
+    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, kWarps * 32, smem) != cudaSuccess)
+      return 1;
+    return std::max(1, n);
+  }
+
+  static cudaError_t launch(const DecodeArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                            cudaStream_t stream) {
+    cudaError_t e;
+    const long long rows = static_cast<long long>(a.batch) * a.num_heads;
+    if (a.persistent_ctas > 0) {
+      auto* k = decode_persistent_kernel<D, BS, kWarps, kStages, FP8>;
+      const int smem = PC::smem_bytes(a.batch);
+      e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      if (e != cudaSuccess) return e;
+      k<<<a.persistent_ctas, kWarps * 32, smem, stream>>>(kmap, vmap, a);
+      if ((e = cudaGetLastError()) != cudaSuccess) return e;
+      decode_persistent_merge_kernel<D><<<static_cast<unsigned>((rows + 3) / 4), 128, 0, stream>>>(
+          a, a.persistent_ctas);
+      return cudaGetLastError();
+    }
+    auto* k = decode_split_kernel<D, BS, kWarps, kStages, FP8>;
+    e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSplitSmem);
+    if (e != cudaSuccess) return e;
+    dim3 grid(a.num_kv_heads, a.batch, a.num_splits);
+    k<<<grid, kWarps * 32, kSplitSmem, stream>>>(kmap, vmap, a);
+    if ((e = cudaGetLastError()) != cudaSuccess || a.num_splits <= 1) return e;
+    decode_split_merge_kernel<D, BS><<<static_cast<unsigned>((rows + 3) / 4), 128, 0, stream>>>(a);
+    return cudaGetLastError();
+  }
+};
 
 int split_tokens_target() {
   static int v = [] {
@@ -487,18 +810,39 @@ int split_tokens_target() {
   return v;
 }
 
+template <typename F>
+auto dispatch(int head_dim, int block_size, bool fp8, F&& f) -> decltype(f(Inst<128, 16, false>{})) {
+  if (fp8) {
+    if (head_dim == 128 && block_size == 16) return f(Inst<128, 16, true>{});
+    return f(Inst<128, 32, true>{});
+  }
+  if (head_dim == 128 && block_size == 16) return f(Inst<128, 16, false>{});
+  if (head_dim == 128 && block_size == 32) return f(Inst<128, 32, false>{});
+  if (head_dim == 64 && block_size == 16) return f(Inst<64, 16, false>{});
+  return f(Inst<64, 32, false>{});
+}
+
 }  // namespace
 
 DecodePlan plan_decode(int batch, int num_heads, int num_kv_heads, int head_dim, int block_size,
                        bool fp8, int len_cap, int num_sms) {
-  (void)fp8;
   DecodePlan p{};
+  const size_t slot_floats = static_cast<size_t>(8) * head_dim + 8 * 2;  // one partial slot
+  if (batch <= kMaxPersistentBatch) {
+    const int per_sm = dispatch(head_dim, block_size, fp8,
+                                [&](auto inst) { return decltype(inst)::ctas_per_sm(batch); });
+    p.persistent_ctas = per_sm * num_sms;
+    p.blocks_per_split = 0;
+    p.num_splits = 0;
+    p.workspace_bytes = 2 * static_cast<size_t>(p.persistent_ctas) * slot_floats * sizeof(float) +
+                        (static_cast<size_t>(batch) + 1) * sizeof(int) + 256;
+    return p;
+  }
+  (void)num_heads;
+  p.persistent_ctas = 0;
   const int max_nblk = (std::max(len_cap, 0) + block_size - 1) / block_size;
   int cb = std::max(1, split_tokens_target() / block_size);
   cb = std::min(cb, 32 * kWarps);  // a warp holds its block ids in one register per lane
-  // Few (sequence, kv head) pairs: cut splits finer so the grid covers the GPU.
-  const long long pairs = static_cast<long long>(batch) * num_kv_heads;
-  while (cb > kWarps && pairs * ((max_nblk + cb - 1) / cb) < 4LL * num_sms) cb >>= 1;
   p.blocks_per_split = cb;
   p.num_splits = std::max(1, (max_nblk + cb - 1) / cb);
   if (p.num_splits > 65535) {  // grid z limit: widen the splits
@@ -508,24 +852,19 @@ DecodePlan plan_decode(int batch, int num_heads, int num_kv_heads, int head_dim,
   if (p.num_splits <= 1) {
     p.workspace_bytes = 0;
   } else {
-    const size_t rows = static_cast<size_t>(batch) * num_heads * p.num_splits;
-    p.workspace_bytes = rows * head_dim * sizeof(float) + rows * 2 * sizeof(float) + 256;
+    const size_t slots = static_cast<size_t>(batch) * num_kv_heads * p.num_splits;
+    p.workspace_bytes = slots * slot_floats * sizeof(float) + 256;
   }
   return p;
 }
 
 cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
                           cudaStream_t stream) {
-  if (a.fp8) {
-    if (a.head_dim == 128 && a.block_size == 16) return launch_t<128, 16, true>(a, kmap, vmap, stream);
-    if (a.head_dim == 128 && a.block_size == 32) return launch_t<128, 32, true>(a, kmap, vmap, stream);
+  if (a.fp8 && a.head_dim != 128) return cudaErrorInvalidValue;
+  if ((a.head_dim != 64 && a.head_dim != 128) || (a.block_size != 16 && a.block_size != 32))
     return cudaErrorInvalidValue;
-  }
-  if (a.head_dim == 128 && a.block_size == 16) return launch_t<128, 16, false>(a, kmap, vmap, stream);
-  if (a.head_dim == 128 && a.block_size == 32) return launch_t<128, 32, false>(a, kmap, vmap, stream);
-  if (a.head_dim == 64 && a.block_size == 16) return launch_t<64, 16, false>(a, kmap, vmap, stream);
-  if (a.head_dim == 64 && a.block_size == 32) return launch_t<64, 32, false>(a, kmap, vmap, stream);
-  return cudaErrorInvalidValue;
+  return dispatch(a.head_dim, a.block_size, a.fp8,
+                  [&](auto inst) { return decltype(inst)::launch(a, kmap, vmap, stream); });
 }
 
 }  // namespace pa

@@ -28,6 +28,10 @@ struct StoreArgs {
 
 cudaError_t launch_store_kv(const StoreArgs& a, cudaStream_t stream);
 
+// Largest batch the persistent decode kernel handles (its per-sequence block
+// prefix sums live in shared memory); larger batches use the grid-split kernel.
+constexpr int kMaxPersistentBatch = 2048;
+
 struct DecodeArgs {
   const void* q;              // (B, H, D) bf16
   const int32_t* block_tables;
@@ -35,18 +39,22 @@ struct DecodeArgs {
   const float* k_scale;       // FP8: (NB, Hkv, bs)
   const float* v_scale;
   void* out;                  // (B, H, D) bf16
-  float* part_o;              // (B, H, S, D) fp32
-  float* part_ml;             // (B, H, S, 2) fp32
+  float* part_o;              // partial slots: (slots, 8, D) fp32
+  float* part_ml;             // (slots, 8, 2) fp32: (max, sum) per head
+  int* prefix_out;            // persistent path: (B+1) block prefix sums for the merge
   uint32_t* err;
   int batch, num_heads, num_kv_heads, group, head_dim, block_size;
   int max_blocks, num_blocks, len_cap;
-  int blocks_per_split, num_splits;
+  int persistent_ctas;        // > 0: persistent kernel with this many CTAs
+  int blocks_per_split, num_splits;  // grid-split path
   bool fp8;
   float scale_log2;
 };
 
-// Split-K plan of a decode call: blocks per split and number of splits.
+// Plan of a decode call: persistent (CTA count, 2 partial slots per CTA) or
+// grid-split (blocks per split, number of splits, one slot per split).
 struct DecodePlan {
+  int persistent_ctas;
   int blocks_per_split;
   int num_splits;
   size_t workspace_bytes;

@@ -148,3 +148,30 @@ def _sampled_full_size(name, n_sample=6):
 def test_full_size_workload_sampled_parity(name):
     got, want = _sampled_full_size(name)
     assert_attention_close(got, want, name)
+
+
+def test_many_short_and_empty_sequences():
+    # many segments per CTA, zero-length sequences in between, tiny pieces
+    gen = torch.Generator().manual_seed(90)
+    lens = torch.randint(0, 60, (300,), generator=gen)
+    lens[::17] = 0
+    lens[5] = 1
+    h = W.make_decode(300, 8, 2, 64, 16, lens.tolist(), seed=91)
+    got, want = run_case(h)
+    assert torch.all(got[lens == 0].float() == 0)
+    assert_attention_close(got, want, "short/empty")
+
+
+def test_one_long_sequence_spread_over_all_ctas():
+    h = W.make_decode(1, 32, 8, 128, 16, [70001], seed=92)
+    got, want = run_case(h, max_context_len=70001)
+    assert_attention_close(got, want, "one long sequence")
+
+
+def test_batch_above_persistent_limit_uses_grid_split():
+    gen = torch.Generator().manual_seed(93)
+    lens = torch.randint(1, 40, (2100,), generator=gen).tolist()
+    lens[7] = 700  # one sequence long enough to need several splits
+    h = W.make_decode(2100, 8, 2, 64, 16, lens, seed=94)
+    got, want = run_case(h, max_context_len=max(lens))
+    assert_attention_close(got, want, "large batch")

@@ -61,7 +61,9 @@ def test_noalloc_matches_decode_on_two_calls_in_a_row(kv):
 
 def test_noalloc_rejects_shapes_beyond_its_scratch():
     g = to_device(W.make_decode(2, 64, 8, 128, 32, [40, 70], seed=71, kv_dtype="fp8"))
-    B, H = 256, 64  # claimed shape: far more split-K scratch than the static buffer
+    # claimed shape: a batch large enough for the grid-split path, whose split-K
+    # scratch grows with batch x context and far exceeds the static buffer
+    B, H = 4096, 64
     need = pa.decode_workspace_size(g.k_cache, B, H, 512, 16384, k_scale=g.k_scale,
                                     v_scale=g.v_scale)
     assert need > pa.DECODE_NOALLOC_SCRATCH_BYTES
