@@ -154,10 +154,11 @@ def decode(q, k_cache, v_cache, block_tables, context_lens, scale: float, *,
     cl = context_lens.contiguous()
     if out is None:
         out = torch.empty((B, H, D), dtype=torch.bfloat16, device=q.device)
-    need = int(lib().pa_decode_workspace_size(ctypes.byref(cache), B, H, bt.shape[1],
-                                              max_context_len))
-    if need and (workspace is None or workspace.numel() * workspace.element_size() < need):
-        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    if workspace is None:  # a caller-provided workspace is checked by the library
+        need = int(lib().pa_decode_workspace_size(ctypes.byref(cache), B, H, bt.shape[1],
+                                                  max_context_len))
+        if need:
+            workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(lib().pa_decode(_ptr(q.contiguous()), ctypes.byref(cache), _ptr(bt), bt.shape[1],
                            _ptr(cl), int(max_context_len), B, H, float(scale), _ptr(out),

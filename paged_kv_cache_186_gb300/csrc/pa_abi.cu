@@ -6,6 +6,7 @@
 
 #include <cmath>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 
 #include "pa.h"
@@ -101,8 +102,55 @@ pa_status encode_cache_map(CUtensorMap* map, void* base, const pa_kv_cache* c) {
   const CUresult r = g_encode(
       map, eb == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base,
       dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+      // rows are head_dim*elem bytes apart from the next head's: promote L2
+      // fills no wider than one row so no neighbouring head is fetched
+      eb == 1 ? CU_TENSOR_MAP_L2_PROMOTION_L2_128B : CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
+}
+
+// Recently encoded cache tensor maps: encoding is pure host work but costs a
+// few microseconds, and a decode loop passes the same cache every step.
+struct MapEntry {
+  void* base;
+  int num_blocks, block_size, num_kv_heads, head_dim, dtype, device;
+  CUtensorMap map;
+};
+constexpr int kMapCache = 16;
+MapEntry g_maps[kMapCache];
+int g_map_count = 0, g_map_next = 0;
+std::mutex g_map_mu;
+
+pa_status cached_cache_map(CUtensorMap* out, void* base, const pa_kv_cache* c) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return PA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_map_mu);
+  for (int i = 0; i < g_map_count; ++i) {
+    const MapEntry& e = g_maps[i];
+    if (e.base == base && e.num_blocks == c->num_blocks && e.block_size == c->block_size &&
+        e.num_kv_heads == c->num_kv_heads && e.head_dim == c->head_dim && e.dtype == c->dtype &&
+        e.device == dev) {
+      *out = e.map;
+      return PA_OK;
+    }
+  }
+  MapEntry e{base, c->num_blocks, c->block_size, c->num_kv_heads, c->head_dim, c->dtype, dev, {}};
+  const pa_status st = encode_cache_map(&e.map, base, c);
+  if (st != PA_OK) return st;
+  g_maps[g_map_next] = e;
+  g_map_next = (g_map_next + 1) % kMapCache;
+  if (g_map_count < kMapCache) ++g_map_count;
+  *out = e.map;
+  return PA_OK;
+}
+
+// Tag of one decode call in the workspace's arrival counters: increasing,
+// never 0 (a zeroed counter never matches the current call).
+uint32_t next_epoch() {
+  static std::atomic<uint32_t> counter{0};
+  uint32_t e = counter.fetch_add(1) + 1;
+  if (e == 0) e = counter.fetch_add(1) + 1;
+  return e;
 }
 
 int decode_len_cap(const pa_kv_cache* c, int32_t max_blocks_per_seq, int32_t max_context_len) {
@@ -204,8 +252,8 @@ pa_status pa_decode(const void* q, const pa_kv_cache* cache, const int32_t* bloc
       (workspace == nullptr || workspace_bytes < plan.workspace_bytes || !aligned16(workspace)))
     return PA_ERR_WORKSPACE;
   CUtensorMap kmap, vmap;
-  if ((st = encode_cache_map(&kmap, cache->k_cache, cache)) != PA_OK) return st;
-  if ((st = encode_cache_map(&vmap, cache->v_cache, cache)) != PA_OK) return st;
+  if ((st = cached_cache_map(&kmap, cache->k_cache, cache)) != PA_OK) return st;
+  if ((st = cached_cache_map(&vmap, cache->v_cache, cache)) != PA_OK) return st;
   pa::DecodeArgs a{};
   a.q = q;
   a.block_tables = block_tables;
@@ -215,11 +263,16 @@ pa_status pa_decode(const void* q, const pa_kv_cache* cache, const int32_t* bloc
   a.out = out;
   if (plan.workspace_bytes > 0) {
     const size_t slots = plan.persistent_ctas > 0
-                             ? 2 * static_cast<size_t>(plan.persistent_ctas)
+                             ? 2 * static_cast<size_t>(plan.persistent_slots_per_cta) *
+                                   plan.persistent_ctas
                              : static_cast<size_t>(batch) * cache->num_kv_heads * plan.num_splits;
     a.part_o = static_cast<float*>(workspace);
     a.part_ml = a.part_o + slots * 8 * cache->head_dim;
     a.prefix_out = reinterpret_cast<int*>(a.part_ml + slots * 8 * 2);
+    // 8-byte aligned arrival counters after the prefix sums
+    const uintptr_t cp = reinterpret_cast<uintptr_t>(a.prefix_out + batch + 1);
+    a.seg_counters = reinterpret_cast<unsigned long long*>((cp + 15) & ~static_cast<uintptr_t>(15));
+    a.epoch = next_epoch();
   }
   a.err = dev->err;
   a.batch = batch;
@@ -280,8 +333,8 @@ pa_status pa_prefill_varlen(const void* q, const pa_kv_cache* cache, const int32
                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return PA_ERR_CUDA;
   }
-  if ((st = encode_cache_map(&kmap, cache->k_cache, cache)) != PA_OK) return st;
-  if ((st = encode_cache_map(&vmap, cache->v_cache, cache)) != PA_OK) return st;
+  if ((st = cached_cache_map(&kmap, cache->k_cache, cache)) != PA_OK) return st;
+  if ((st = cached_cache_map(&vmap, cache->v_cache, cache)) != PA_OK) return st;
   pa::PrefillArgs a{};
   a.block_tables = block_tables;
   a.cu_q = cu_seqlens_q;

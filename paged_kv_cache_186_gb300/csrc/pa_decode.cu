@@ -11,12 +11,12 @@
 // How (GB300 design):
 //   * Work is the list of (sequence, kv head) "segments", each a run of
 //     ceil(context_len / bs) physical blocks. The persistent kernel gives every
-//     CTA an equal contiguous share of all blocks of all segments (a balanced
+//     warp an equal contiguous share of all blocks of all segments (a balanced
 //     split: long and short sequences cost the same per block, and no CTA is
-//     launched without work). A segment that straddles CTAs is finished by a
-//     small merge kernel from at most two partial results per CTA.
-//   * A CTA's warps take the blocks of each segment piece round-robin; all
-//     G = H/Hkv query heads of the kv head share every K/V tile (GQA).
+//     launched without work). A warp writes the bf16 rows of a segment it holds
+//     whole; for a segment that straddles warps each writes an fp32 partial
+//     and the last to arrive (per-segment counter) merges them.
+//   * All G = H/Hkv query heads of a kv head share every K/V tile (GQA).
 //   * Each warp streams its blocks through a private ring of shared-memory
 //     stages filled by TMA (3-D tiled loads of one block of one kv head,
 //     128B-swizzled; FP8 scales by 1-D bulk copies), tracked by mbarriers with
@@ -28,8 +28,6 @@
 //     ("tiny-vllm part 05", pagedAttentionKernel section): a running max and
 //     sum per head, reduced over the 4 lanes that share a head with warp
 //     shuffles, accumulators rescaled when the max grows.
-//   * At the end of each segment piece the warps merge (max, sum, O) in shared
-//     memory; a segment that lies inside one CTA writes bf16 output directly.
 //   * FP8-E4M3 KV: codes are widened exactly to f16 in registers; the K scale
 //     multiplies the score, the V scale multiplies the probability.
 //   * Batches above kMaxPersistentBatch use a grid of (kv head, sequence,
@@ -45,6 +43,7 @@ namespace pa {
 namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
+constexpr int kMaxDevices = 64;
 
 template <int D, int BS, int NW, int ST, bool FP8>
 struct Cfg {
@@ -108,81 +107,91 @@ __device__ __forceinline__ void load_q(const DecodeArgs& a, int b, int kvh, int 
 // One physical block (tokens tok0 .. tok0+BS-1, of which those < L count)
 // staged in shared memory at kt (K) / vt (V), FP8 scales at ksc / vsc:
 // fold it into the warp's online-softmax state (m_run, l_run for head r of
-// lane group r; acc = O^T fragments for heads 2q4, 2q4+1).
+// lane group r; acc = O^T fragments for heads 2q4, 2q4+1). The whole block is
+// one softmax step: S for its BS tokens (BS/8 n-tiles, independent MMA
+// chains), one max/sum update, then P.V per 16-token group.
 template <int D, int BS, bool FP8>
 __device__ __forceinline__ void attend_block(uint32_t kt, uint32_t vt, const uint8_t* base_ptr,
                                              uint32_t base, const float* ksc, const float* vsc,
                                              int tok0, int L, const uint32_t (&qa)[D / 16][2],
                                              float (&acc)[D / 16][4], float& m_run, float& l_run,
                                              float sl2, int lane) {
+  constexpr int NT = BS / 8;  // n-tiles of 8 tokens
+  constexpr int NG = BS / 16;  // 16-token groups (k-steps of P.V)
   const int r = lane >> 2, q4 = lane & 3;
+  const bool partial = tok0 + BS > L;
+  // ---- S = Q K^T for the block's tokens
+  float sc[NT][4];
 #pragma unroll
-  for (int hf = 0; hf < BS / 16; ++hf) {
-    const int htok = tok0 + hf * 16;
-    if (htok >= L) break;
-    const bool partial = htok + 16 > L;
-    // ---- S = Q K^T for 16 tokens (two n-tiles of 8)
-    float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-    if constexpr (!FP8) {
-      const int mi = lane >> 3;
-      const int row = hf * 16 + (mi >> 1) * 8 + (lane & 7);
+  for (int nt = 0; nt < NT; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+  if constexpr (!FP8) {
+    const int mi = lane >> 3;
 #pragma unroll
-      for (int ks = 0; ks < D / 16; ++ks) {
+    for (int ks = 0; ks < D / 16; ++ks) {
+#pragma unroll
+      for (int hg = 0; hg < NG; ++hg) {
+        const int row = hg * 16 + (mi >> 1) * 8 + (lane & 7);
         uint32_t b00, b01, b10, b11;
         ldmatrix_x4(swz<BS>(kt, row, 2 * ks + (mi & 1)), b00, b01, b10, b11);
-        mma_bf16(sc[0], qa[ks][0], 0u, qa[ks][1], 0u, b00, b01);
-        mma_bf16(sc[1], qa[ks][0], 0u, qa[ks][1], 0u, b10, b11);
-      }
-    } else {
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
-        const int row = hf * 16 + nt * 8 + r;
-        uint32_t w[8];
-        const uint4 c0 =
-            *reinterpret_cast<const uint4*>(base_ptr + (swz<BS>(kt, row, 2 * q4) - base));
-        const uint4 c1 =
-            *reinterpret_cast<const uint4*>(base_ptr + (swz<BS>(kt, row, 2 * q4 + 1) - base));
-        w[0] = c0.x; w[1] = c0.y; w[2] = c0.z; w[3] = c0.w;
-        w[4] = c1.x; w[5] = c1.y; w[6] = c1.z; w[7] = c1.w;
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks)
-          mma_f16(sc[nt], qa[ks][0], 0u, qa[ks][1], 0u, e4m3x2_to_f16x2(w[ks] & 0xffffu),
-                  e4m3x2_to_f16x2(w[ks] >> 16));
+        mma_bf16(sc[2 * hg], qa[ks][0], 0u, qa[ks][1], 0u, b00, b01);
+        mma_bf16(sc[2 * hg + 1], qa[ks][0], 0u, qa[ks][1], 0u, b10, b11);
       }
     }
-    // ---- online softmax for head r over tokens htok + nt*8 + 2q4 + {0,1}
-    float x[4];
+  } else {
+    uint32_t w[NT][8];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const int row = nt * 8 + r;
+      const uint4 c0 = *reinterpret_cast<const uint4*>(base_ptr + (swz<BS>(kt, row, 2 * q4) - base));
+      const uint4 c1 =
+          *reinterpret_cast<const uint4*>(base_ptr + (swz<BS>(kt, row, 2 * q4 + 1) - base));
+      w[nt][0] = c0.x; w[nt][1] = c0.y; w[nt][2] = c0.z; w[nt][3] = c0.w;
+      w[nt][4] = c1.x; w[nt][5] = c1.y; w[nt][6] = c1.z; w[nt][7] = c1.w;
+    }
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        uint32_t b0, b1;
+        e4m3x4_to_f16x2x2(w[nt][ks], b0, b1);
+        mma_f16(sc[nt], qa[ks][0], 0u, qa[ks][1], 0u, b0, b1);
+      }
+    }
+  }
+  // ---- one online-softmax step for head r over tokens tok0 + nt*8 + 2q4 + {0,1}
+  float x[2 * NT];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
     if constexpr (!FP8) {
-      x[0] = sc[0][0] * sl2;
-      x[1] = sc[0][1] * sl2;
-      x[2] = sc[1][0] * sl2;
-      x[3] = sc[1][1] * sl2;
+      x[2 * nt] = sc[nt][0] * sl2;
+      x[2 * nt + 1] = sc[nt][1] * sl2;
     } else {
-      const float2 k0 = *reinterpret_cast<const float2*>(ksc + hf * 16 + 2 * q4);
-      const float2 k1 = *reinterpret_cast<const float2*>(ksc + hf * 16 + 8 + 2 * q4);
-      x[0] = sc[0][0] * (k0.x * sl2);
-      x[1] = sc[0][1] * (k0.y * sl2);
-      x[2] = sc[1][0] * (k1.x * sl2);
-      x[3] = sc[1][1] * (k1.y * sl2);
+      const float2 k2 = *reinterpret_cast<const float2*>(ksc + nt * 8 + 2 * q4);
+      x[2 * nt] = sc[nt][0] * (k2.x * sl2);
+      x[2 * nt + 1] = sc[nt][1] * (k2.y * sl2);
     }
-    bool valid[4] = {true, true, true, true};
-    if (partial) {
+  }
+  if (partial) {
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        valid[j] = htok + (j >> 1) * 8 + 2 * q4 + (j & 1) < L;
-        if (!valid[j]) x[j] = -INFINITY;
-      }
-    }
-    float mx = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
-    mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 1));
-    mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 2));
-    const float m_new = fmaxf(m_run, mx);
+    for (int j = 0; j < 2 * NT; ++j)
+      if (tok0 + (j >> 1) * 8 + 2 * q4 + (j & 1) >= L) x[j] = -INFINITY;
+  }
+  float mx = x[0];
+#pragma unroll
+  for (int j = 1; j < 2 * NT; ++j) mx = fmaxf(mx, x[j]);
+  mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 1));
+  mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 2));
+  const float m_new = fmaxf(m_run, mx);
+  float pr[2 * NT];
+  float psum = 0.f;
+#pragma unroll
+  for (int j = 0; j < 2 * NT; ++j) {
+    pr[j] = fast_exp2(x[j] - m_new);
+    psum += pr[j];
+  }
+  if (__any_sync(kFull, m_new > m_run)) {  // some head's max grew: rescale
     const float alpha = fast_exp2(m_run - m_new);
-    float pr[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) pr[j] = fast_exp2(x[j] - m_new);
-    l_run = l_run * alpha + ((pr[0] + pr[1]) + (pr[2] + pr[3]));
-    m_run = m_new;
+    l_run *= alpha;
     // accumulator columns are heads 2q4 and 2q4+1: fetch their factors
     const float al0 = __shfl_sync(kFull, alpha, 8 * q4);
     const float al1 = __shfl_sync(kFull, alpha, 8 * q4 + 4);
@@ -193,32 +202,49 @@ __device__ __forceinline__ void attend_block(uint32_t kt, uint32_t vt, const uin
       acc[mt][2] *= al0;
       acc[mt][3] *= al1;
     }
-    // token-validity masks for the V^T fragments (lo half = token 2q4(+8))
-    uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;
-    if (partial) {
-      mlo = (valid[0] ? 0x0000ffffu : 0u) | (valid[1] ? 0xffff0000u : 0u);
-      mhi = (valid[2] ? 0x0000ffffu : 0u) | (valid[3] ? 0xffff0000u : 0u);
-    }
-    // ---- O^T += V^T P^T
-    if constexpr (!FP8) {
-      const uint32_t pb0 = pack_bf16x2(pr[0], pr[1]);
-      const uint32_t pb1 = pack_bf16x2(pr[2], pr[3]);
-      const int mi = lane >> 3;
-      const int row = hf * 16 + (mi >> 1) * 8 + (lane & 7);
+  }
+  l_run += psum;
+  m_run = m_new;
+  // ---- O^T += V^T P^T, one k-step per 16-token group
 #pragma unroll
-      for (int mt = 0; mt < D / 16; ++mt) {
-        uint32_t a0, a1, a2, a3;
-        ldmatrix_x4_trans(swz<BS>(vt, row, 2 * mt + (mi & 1)), a0, a1, a2, a3);
-        mma_bf16(acc[mt], a0 & mlo, a1 & mlo, a2 & mhi, a3 & mhi, pb0, pb1);
+  for (int hg = 0; hg < NG; ++hg) {
+    const int g0 = tok0 + hg * 16 + 2 * q4;  // tokens of this lane's P entries: g0, g0+1, g0+8, g0+9
+    if (partial && hg * 16 + tok0 >= L) break;
+    uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;
+    if (partial) {  // V rows past the sequence may hold anything: zero their fragments
+      mlo = (g0 < L ? 0x0000ffffu : 0u) | (g0 + 1 < L ? 0xffff0000u : 0u);
+      mhi = (g0 + 8 < L ? 0x0000ffffu : 0u) | (g0 + 9 < L ? 0xffff0000u : 0u);
+    }
+    const float p0 = pr[4 * hg], p1 = pr[4 * hg + 1], p8 = pr[4 * hg + 2], p9 = pr[4 * hg + 3];
+    if constexpr (!FP8) {
+      const uint32_t pb0 = pack_bf16x2(p0, p1);
+      const uint32_t pb1 = pack_bf16x2(p8, p9);
+      const int mi = lane >> 3;
+      const int row = hg * 16 + (mi >> 1) * 8 + (lane & 7);
+      if (partial) {
+#pragma unroll
+        for (int mt = 0; mt < D / 16; ++mt) {
+          uint32_t a0, a1, a2, a3;
+          ldmatrix_x4_trans(swz<BS>(vt, row, 2 * mt + (mi & 1)), a0, a1, a2, a3);
+          mma_bf16(acc[mt], a0 & mlo, a1 & mlo, a2 & mhi, a3 & mhi, pb0, pb1);
+        }
+      } else {
+#pragma unroll
+        for (int mt = 0; mt < D / 16; ++mt) {
+          uint32_t a0, a1, a2, a3;
+          ldmatrix_x4_trans(swz<BS>(vt, row, 2 * mt + (mi & 1)), a0, a1, a2, a3);
+          mma_bf16(acc[mt], a0, a1, a2, a3, pb0, pb1);
+        }
       }
     } else {
-      const float2 v0 = *reinterpret_cast<const float2*>(vsc + hf * 16 + 2 * q4);
-      const float2 v1 = *reinterpret_cast<const float2*>(vsc + hf * 16 + 8 + 2 * q4);
-      const uint32_t pb0 = pack_f16x2(valid[0] ? pr[0] * v0.x : 0.f, valid[1] ? pr[1] * v0.y : 0.f);
-      const uint32_t pb1 = pack_f16x2(valid[2] ? pr[2] * v1.x : 0.f, valid[3] ? pr[3] * v1.y : 0.f);
+      const float2 v0 = *reinterpret_cast<const float2*>(vsc + hg * 16 + 2 * q4);
+      const float2 v1 = *reinterpret_cast<const float2*>(vsc + hg * 16 + 8 + 2 * q4);
+      // masked tokens have p = 0 but their scales may be anything: select, not multiply
+      const uint32_t pb0 = pack_f16x2(g0 < L ? p0 * v0.x : 0.f, g0 + 1 < L ? p1 * v0.y : 0.f);
+      const uint32_t pb1 = pack_f16x2(g0 + 8 < L ? p8 * v1.x : 0.f, g0 + 9 < L ? p9 * v1.y : 0.f);
       // lane (r, q4) reads 16-byte chunk r of token rows 2q4, 2q4+1, 2q4+8, 2q4+9:
-      // word w gives dims 16r + 4w + {0..3}; output row mapping in store_warp_state.
-      const int t0 = hf * 16 + 2 * q4;
+      // word w gives dims 16r + 4w + {0..3}; output row mapping in the writers.
+      const int t0 = hg * 16 + 2 * q4;
       const uint4 W0 = *reinterpret_cast<const uint4*>(base_ptr + (swz<BS>(vt, t0, r) - base));
       const uint4 W1 = *reinterpret_cast<const uint4*>(base_ptr + (swz<BS>(vt, t0 + 1, r) - base));
       const uint4 W8 = *reinterpret_cast<const uint4*>(base_ptr + (swz<BS>(vt, t0 + 8, r) - base));
@@ -232,12 +258,15 @@ __device__ __forceinline__ void attend_block(uint32_t kt, uint32_t vt, const uin
 #pragma unroll
         for (int o = 0; o < 2; ++o) {
           const uint32_t sel = o ? 0x7362u : 0x5140u;
-          const uint32_t p01 = prmt(w0[w], w1[w], sel);
-          const uint32_t p89 = prmt(w8[w], w9[w], sel);
-          const uint32_t a0 = e4m3x2_to_f16x2(p01 & 0xffffu) & mlo;
-          const uint32_t a1 = e4m3x2_to_f16x2(p01 >> 16) & mlo;
-          const uint32_t a2 = e4m3x2_to_f16x2(p89 & 0xffffu) & mhi;
-          const uint32_t a3 = e4m3x2_to_f16x2(p89 >> 16) & mhi;
+          uint32_t a0, a1, a2, a3;
+          e4m3x4_to_f16x2x2(prmt(w0[w], w1[w], sel), a0, a1);
+          e4m3x4_to_f16x2x2(prmt(w8[w], w9[w], sel), a2, a3);
+          if (partial) {
+            a0 &= mlo;
+            a1 &= mlo;
+            a2 &= mhi;
+            a3 &= mhi;
+          }
           mma_f16(acc[2 * w + o], a0, a1, a2, a3, pb0, pb1);
         }
       }
@@ -317,10 +346,11 @@ __device__ __forceinline__ void merge_warps_and_write(const float* mo, const Dec
 
 // ============================================================ persistent path
 // Flattened work: segment (b, kvh) in b-major order holds nblk(b) blocks; the
-// global index of its first block is prefix[b] * Hkv + kvh * nblk(b). CTA c of
-// P owns [c*N/P, (c+1)*N/P) with N = prefix[B] * Hkv.
+// global index of its first block is prefix[b] * Hkv + kvh * nblk(b). Warp w
+// of all W = gridDim.x * NW warps owns blocks [w*N/W, (w+1)*N/W) with
+// N = prefix[B] * Hkv: equal work per warp whatever the length mix.
 struct Piece {
-  int b, kvh, lo, hi;  // segment and its block range owned by this CTA
+  int b, kvh, lo, hi;  // segment and its block range owned by this warp
   int nblk;            // blocks of the segment
   long long g;         // global index of block `lo`
   bool valid;
@@ -363,18 +393,205 @@ __device__ __forceinline__ void piece_next(Piece& p, const int* prefix, int B, i
   p.hi = static_cast<int>(min(static_cast<long long>(p.nblk), r1 - p.g));
 }
 
+// Write the warp's result for segment (b, kvh): bf16 output rows if the
+// segment is entirely this warp's, else an fp32 partial (O unnormalised,
+// (max, sum) per head) in `slot`. Lane (r, q4) holds O^T for heads 2q4, 2q4+1
+// and the running max/sum of head r.
+template <int D, bool FP8>
+__device__ __forceinline__ void write_warp_result(const DecodeArgs& a, int b, int kvh,
+                                                  bool final_out, long long slot, int lane,
+                                                  float m_run, float l_run,
+                                                  const float (&acc)[D / 16][4]) {
+  const int r = lane >> 2, q4 = lane & 3, G = a.group;
+  float l_tot = l_run + __shfl_xor_sync(kFull, l_run, 1);
+  l_tot += __shfl_xor_sync(kFull, l_tot, 2);
+  const int h0 = 2 * q4, h1 = 2 * q4 + 1;  // accumulator heads of this lane
+  const float l0 = __shfl_sync(kFull, l_tot, 4 * h0);
+  const float l1 = __shfl_sync(kFull, l_tot, 4 * h1);
+  if (final_out) {
+    const float inv0 = l0 > 0.f ? 1.f / l0 : 0.f, inv1 = l1 > 0.f ? 1.f / l1 : 0.f;
+    __nv_bfloat16* o = static_cast<__nv_bfloat16*>(a.out) +
+                       (static_cast<long long>(b) * a.num_heads + kvh * G) * D;
+#pragma unroll
+    for (int mt = 0; mt < D / 16; ++mt) {
+      int d0, d1;
+      if constexpr (!FP8) { d0 = mt * 16 + r; d1 = d0 + 8; }
+      else { d0 = 16 * r + 4 * (mt >> 1) + 2 * (mt & 1); d1 = d0 + 1; }
+      if (h0 < G) {
+        o[h0 * D + d0] = __float2bfloat16_rn(acc[mt][0] * inv0);
+        o[h0 * D + d1] = __float2bfloat16_rn(acc[mt][2] * inv0);
+      }
+      if (h1 < G) {
+        o[h1 * D + d0] = __float2bfloat16_rn(acc[mt][1] * inv1);
+        o[h1 * D + d1] = __float2bfloat16_rn(acc[mt][3] * inv1);
+      }
+    }
+    return;
+  }
+  float* po = a.part_o + slot * 8 * D;
+#pragma unroll
+  for (int mt = 0; mt < D / 16; ++mt) {
+    int d0, d1;
+    if constexpr (!FP8) { d0 = mt * 16 + r; d1 = d0 + 8; }
+    else { d0 = 16 * r + 4 * (mt >> 1) + 2 * (mt & 1); d1 = d0 + 1; }
+    if (h0 < G) {
+      po[h0 * D + d0] = acc[mt][0];
+      po[h0 * D + d1] = acc[mt][2];
+    }
+    if (h1 < G) {
+      po[h1 * D + d0] = acc[mt][1];
+      po[h1 * D + d1] = acc[mt][3];
+    }
+  }
+  if (q4 == 0 && r < G) {
+    a.part_ml[(slot * 8 + r) * 2 + 0] = m_run;
+    a.part_ml[(slot * 8 + r) * 2 + 1] = l_tot;
+  }
+}
+
+// Warps that take part: at most one per kMinBlocksPerWarp blocks of work, so
+// that every active warp owns a non-empty range.
+constexpr int kMinBlocksPerWarp = 4;
+
+// Pieces of a segment that straddles warps: segment (b, kvh) over global
+// blocks [s0, s1) is split among warps w0 .. w1 (all with non-empty ranges);
+// warp w0 left its piece in slot 2*w0+1, every later one in slot 2*w.
+struct SegParts {
+  long long w0;
+  int n;  // w1 - w0 + 1
+  __device__ __forceinline__ long long slot(int j) const {
+    return j == 0 ? 2 * w0 + 1 : 2 * (w0 + j);
+  }
+};
+
+__device__ __forceinline__ SegParts seg_parts(const int* prefix, int B, int Hkv, int b, int kvh,
+                                              long long W) {
+  const long long N = static_cast<long long>(prefix[B]) * Hkv;
+  const int nblk = prefix[b + 1] - prefix[b];
+  const long long s0 = static_cast<long long>(prefix[b]) * Hkv + static_cast<long long>(kvh) * nblk;
+  auto owner = [&](long long x) { return ((x + 1) * W - 1) / N; };
+  SegParts sp;
+  sp.w0 = owner(s0);
+  sp.n = static_cast<int>(owner(s0 + nblk - 1) - sp.w0 + 1);
+  return sp;
+}
+
+// Count this warp's arrival at segment `seg` (64-bit counter: call epoch in
+// the high word, arrivals of that call in the low word; a counter left by an
+// earlier call restarts at 1). Returns true for the last of `parts` arrivals.
+__device__ __forceinline__ bool arrive_last(unsigned long long* counter, uint32_t epoch,
+                                            uint32_t parts, uint32_t* err) {
+  unsigned long long old = atomicAdd(counter, 0ull);
+#pragma unroll 1
+  for (int it = 0; it < (1 << 20); ++it) {
+    const unsigned long long nv = (static_cast<uint32_t>(old >> 32) == epoch)
+                                      ? old + 1
+                                      : ((static_cast<unsigned long long>(epoch) << 32) | 1ull);
+    const unsigned long long prev = atomicCAS(counter, old, nv);
+    if (prev == old) return static_cast<uint32_t>(nv) == parts;
+    old = prev;
+  }
+  report_error(err, PA_DEVERR_WAIT_TIMEOUT);
+  return false;
+}
+
+// Merge the partials of segment (b, kvh) and write its bf16 rows:
+// M = max m_j, l = sum l_j 2^(m_j - M), o = sum o_j 2^(m_j - M) / l (scores in
+// base 2), for all G heads at once. Lane = (part j, head g) with GP lanes per
+// part (G rounded up to a power of two): one round of loads gives every
+// (max, sum), combined online within a lane and across lanes by shuffles;
+// then each lane accumulates D/32 dims of every head over the parts with
+// independent loads. Partials are read through L2.
+template <int D, int GP>
+__device__ __forceinline__ void merge_segment_g(const DecodeArgs& a, const SegParts& sp, int b,
+                                                int kvh, int lane) {
+  constexpr int V = D / 32;
+  constexpr int PR = 32 / GP;  // parts per round
+  const int G = a.group;
+  const int j_l = lane / GP, g_l = lane % GP;
+  const bool g_ok = g_l < G;
+  // ---- (max, sum) per head, online over rounds and lanes
+  float M = -INFINITY, L = 0.f;
+  for (int j0 = 0; j0 < sp.n; j0 += PR) {
+    const int j = j0 + j_l;
+    if (j < sp.n && g_ok) {
+      const float2 ml = __ldcg(reinterpret_cast<const float2*>(a.part_ml + (sp.slot(j) * 8 + g_l) * 2));
+      const float m2 = fmaxf(M, ml.x);
+      L = L * fast_exp2(M - m2) + ml.y * fast_exp2(ml.x - m2);
+      M = m2;
+    }
+  }
+#pragma unroll
+  for (int o = 16; o >= GP; o >>= 1) {
+    const float Mo = __shfl_xor_sync(kFull, M, o), Lo = __shfl_xor_sync(kFull, L, o);
+    const float m2 = fmaxf(M, Mo);
+    if (m2 != -INFINITY) {
+      L = L * fast_exp2(M - m2) + Lo * fast_exp2(Mo - m2);
+      M = m2;
+    }
+  }
+  // ---- outputs: lane holds dims lane*V .. +V-1 of every head
+  float acc[GP][V];
+#pragma unroll
+  for (int g = 0; g < GP; ++g)
+#pragma unroll
+    for (int v = 0; v < V; ++v) acc[g][v] = 0.f;
+  for (int j0 = 0; j0 < sp.n; j0 += PR) {
+    float f = 0.f;
+    const int j = j0 + j_l;
+    if (j < sp.n && g_ok) f = fast_exp2(__ldcg(a.part_ml + (sp.slot(j) * 8 + g_l) * 2) - M);
+#pragma unroll
+    for (int jj = 0; jj < PR; ++jj) {
+#pragma unroll
+      for (int g = 0; g < GP; ++g) {
+        const float fv = __shfl_sync(kFull, f, jj * GP + g);
+        if (j0 + jj < sp.n && g < G) {
+          const float* src = a.part_o + (sp.slot(j0 + jj) * 8 + g) * D + lane * V;
+          if constexpr (V == 4) {
+            const float4 x = __ldcg(reinterpret_cast<const float4*>(src));
+            acc[g][0] += fv * x.x; acc[g][1] += fv * x.y; acc[g][2] += fv * x.z; acc[g][3] += fv * x.w;
+          } else {
+            const float2 x = __ldcg(reinterpret_cast<const float2*>(src));
+            acc[g][0] += fv * x.x; acc[g][1] += fv * x.y;
+          }
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int g = 0; g < GP; ++g) {
+    const float lg = __shfl_sync(kFull, L, g);
+    if (g < G) {
+      const float inv = lg > 0.f ? 1.f / lg : 0.f;
+      __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.out) +
+                           (static_cast<long long>(b) * a.num_heads + kvh * G + g) * D + lane * V;
+#pragma unroll
+      for (int v = 0; v < V; v += 2)
+        *reinterpret_cast<__nv_bfloat162*>(dst + v) =
+            __floats2bfloat162_rn(acc[g][v] * inv, acc[g][v + 1] * inv);
+    }
+  }
+}
+
+template <int D>
+__device__ __forceinline__ void merge_segment(const DecodeArgs& a, const SegParts& sp, int b,
+                                              int kvh, int lane) {
+  if (a.group <= 1) merge_segment_g<D, 1>(a, sp, b, kvh, lane);
+  else if (a.group <= 2) merge_segment_g<D, 2>(a, sp, b, kvh, lane);
+  else if (a.group <= 4) merge_segment_g<D, 4>(a, sp, b, kvh, lane);
+  else merge_segment_g<D, 8>(a, sp, b, kvh, lane);
+}
+
 template <int D, int BS, int NW, int ST, bool FP8>
 struct PCfg {
   using C = Cfg<D, BS, NW, ST, FP8>;
-  static constexpr int kRings = C::kTiles;
-  static constexpr int kScaleOff = kRings;
-  static constexpr int kMergeOff = kScaleOff + C::kScaleBytes;
-  static constexpr int kPrefixOff = kMergeOff + 2 * C::kMerge;
+  static constexpr int kScaleOff = C::kTiles;
+  static constexpr int kPrefixOff = kScaleOff + C::kScaleBytes;
   static int smem_bytes(int batch) { return 1024 + kPrefixOff + (batch + 1) * 4; }
 };
 
 template <int D, int BS, int NW, int ST, bool FP8>
-__global__ void __launch_bounds__(NW * 32)
+__global__ void __launch_bounds__(NW * 32, 3)
     decode_persistent_kernel(const __grid_constant__ CUtensorMap kmap,
                              const __grid_constant__ CUtensorMap vmap, const DecodeArgs a) {
   using C = Cfg<D, BS, NW, ST, FP8>;
@@ -388,12 +605,14 @@ __global__ void __launch_bounds__(NW * 32)
   uint8_t* const base_ptr = smem_raw + (base - raw);
   const uint32_t scale_base = base + PC::kScaleOff;
   const float* const scale_ptr = reinterpret_cast<const float*>(base_ptr + PC::kScaleOff);
-  float* const merge_buf = reinterpret_cast<float*>(base_ptr + PC::kMergeOff);
   int* const prefix = reinterpret_cast<int*>(base_ptr + PC::kPrefixOff);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int B = a.batch, Hkv = a.num_kv_heads;
-  const int c = blockIdx.x, P = gridDim.x;
+  // Launched as a programmatic dependent: everything this kernel reads (the
+  // lengths, block table, q, the cache) may be written by the kernel before
+  // it on the stream, so wait for it before the first read.
+  grid_dependency_wait();
 
   // ---- blocks per sequence and their exclusive prefix sum (whole CTA)
   int carry = 0;
@@ -420,12 +639,23 @@ __global__ void __launch_bounds__(NW * 32)
   }
   if (threadIdx.x == 0) prefix[B] = carry;
   __syncthreads();
-  if (c == 0)
-    for (int i = threadIdx.x; i <= B; i += NW * 32) a.prefix_out[i] = prefix[i];
+  if (blockIdx.x == 0) {
+    // sequences without keys: zero output rows (no warp owns any of their blocks)
+    for (int i = threadIdx.x; i < B * a.num_heads * (D / 8); i += NW * 32) {
+      const int row = i / (D / 8), b = row / a.num_heads;
+      if (prefix[b + 1] == prefix[b])
+        reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) +
+                                 static_cast<long long>(row) * D)[i % (D / 8)] = make_uint4(0, 0, 0, 0);
+    }
+  }
 
+  // ---- this warp's range; from here on warps are independent
   const long long N = static_cast<long long>(prefix[B]) * Hkv;
-  const long long r0 = c * N / P, r1 = (c + 1) * N / P;
-  if (r0 >= r1) return;  // whole CTA: no work
+  const long long W = max(1LL, min(static_cast<long long>(gridDim.x) * NW, N / kMinBlocksPerWarp));
+  const long long gw = static_cast<long long>(blockIdx.x) * NW + warp;
+  if (gw >= W) return;
+  const long long r0 = gw * N / W, r1 = (gw + 1) * N / W;
+  if (r0 >= r1) return;
 
   const uint32_t bar0 = smem_addr(&bars[warp * ST]);
   const uint32_t stage0 = base + warp * ST * C::kStage;
@@ -436,24 +666,25 @@ __global__ void __launch_bounds__(NW * 32)
   }
   __syncwarp();
 
-  // ---- producer: this warp's blocks in order, across pieces
+  // ---- producer: this warp's blocks in order across pieces; the block id of
+  // the next load is fetched one step before it is needed
   Piece pp;
   piece_first(pp, prefix, B, Hkv, r0, r1);
-  int pp_next = pp.lo + warp;
+  int pp_next = pp.lo;
   bool pend = false;
   int pend_kvh = 0, pend_phys = 0;
-  auto fetch_next = [&]() {  // find the next block of this warp, start loading its id
+  auto fetch_next = [&]() {
     pend = false;
     while (pp.valid) {
       if (pp_next < pp.hi) {
         pend = true;
         pend_kvh = pp.kvh;
         pend_phys = a.block_tables[static_cast<long long>(pp.b) * a.max_blocks + pp_next];
-        pp_next += NW;
+        ++pp_next;
         return;
       }
       piece_next(pp, prefix, B, Hkv, r1);
-      pp_next = pp.lo + warp;
+      pp_next = pp.lo;
     }
   };
   int issued = 0;
@@ -489,13 +720,13 @@ __global__ void __launch_bounds__(NW * 32)
   fetch_next();
   for (int s = 0; s < ST; ++s) issue_pending();
 
-  // ---- consumer: pieces in order; all warps meet at each piece end
+  // ---- consumer: pieces in order
   Piece cp;
   piece_first(cp, prefix, B, Hkv, r0, r1);
   const float sl2 = a.scale_log2;
-  int consumed = 0, piece_idx = 0;
+  int consumed = 0;
   bool ok = true;
-  while (cp.valid) {
+  while (ok && cp.valid) {
     uint32_t qa[D / 16][2];
     load_q<D, FP8>(a, cp.b, cp.kvh, lane, qa);
     const int L = min(max(a.context_lens[cp.b], 0), a.len_cap);
@@ -503,7 +734,7 @@ __global__ void __launch_bounds__(NW * 32)
 #pragma unroll
     for (int mt = 0; mt < D / 16; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
     float m_run = -INFINITY, l_run = 0.f;
-    for (int blk = cp.lo + warp; ok && blk < cp.hi; blk += NW) {
+    for (int blk = cp.lo; blk < cp.hi; ++blk) {
       const int s = consumed % ST;
       const bool got = mbar_wait(bar0 + 8 * s, (consumed / ST) & 1);
       if (!__all_sync(kFull, got)) {
@@ -519,74 +750,30 @@ __global__ void __launch_bounds__(NW * 32)
       __syncwarp();
       issue_pending();
     }
-    float* mo = merge_buf + (piece_idx & 1) * (C::kMerge / 4);
-    store_warp_state<D, NW, FP8>(mo, warp, lane, m_run, l_run, acc);
-    // all warps of the CTA: every one walks the same pieces
-    asm volatile("bar.sync 1, %0;" ::"n"(NW * 32) : "memory");
+    if (!ok) break;
     const bool whole = cp.lo == 0 && cp.hi == cp.nblk;
-    const long long slot = 2LL * c + (cp.lo == 0 ? 1 : 0);
-    if (ok) merge_warps_and_write<D, NW>(mo, a, cp.b, cp.kvh, whole, slot);
-    ++piece_idx;
+    write_warp_result<D, FP8>(a, cp.b, cp.kvh, whole, 2 * gw + (cp.lo == 0 ? 1 : 0), lane, m_run,
+                              l_run, acc);
+    if (!whole) {
+      // publish the partial, count the arrival; the last warp merges the segment
+      __threadfence();
+      __syncwarp();
+      const SegParts sp = seg_parts(prefix, B, Hkv, cp.b, cp.kvh, W);
+      int last = 0;
+      if (lane == 0)
+        last = arrive_last(a.seg_counters + static_cast<long long>(cp.b) * Hkv + cp.kvh, a.epoch,
+                           static_cast<uint32_t>(sp.n), a.err);
+      if (__shfl_sync(kFull, last, 0)) {
+        __threadfence();
+        merge_segment<D>(a, sp, cp.b, cp.kvh, lane);
+      }
+    }
     piece_next(cp, prefix, B, Hkv, r1);
   }
   if (!ok) {
     // give copies still in flight a bounded chance to land before exit
     for (int i = consumed; i < issued; ++i) (void)mbar_wait(bar0 + 8 * (i % ST), (i / ST) & 1);
   }
-}
-
-// Finish segments that straddle CTAs: for segment (b, kvh) over global blocks
-// [s0, s1), CTA owner(s0) left its piece in slot 2*owner(s0)+1 and every
-// later CTA up to owner(s1-1) (with a non-empty range) in slot 2*c. Merge:
-// M = max m_j, l = sum l_j 2^(m_j - M), o = sum o_j 2^(m_j - M) / l (base-2
-// scores). Sequences with no keys get zero rows. One warp per (b, query head).
-template <int D>
-__global__ void __launch_bounds__(128) decode_persistent_merge_kernel(const DecodeArgs a, int P) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const long long gw = static_cast<long long>(blockIdx.x) * 4 + warp;
-  if (gw >= static_cast<long long>(a.batch) * a.num_heads) return;
-  const int b = static_cast<int>(gw / a.num_heads);
-  const int h = static_cast<int>(gw % a.num_heads);
-  const int G = a.group, kvh = h / G, g = h % G, Hkv = a.num_kv_heads;
-  const int* prefix = a.prefix_out;
-  const int nblk = prefix[b + 1] - prefix[b];
-  constexpr int V = D / 32;  // dims per lane
-  __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.out) + gw * D + lane * V;
-  if (nblk == 0) {
-#pragma unroll
-    for (int v = 0; v < V; v += 2)
-      *reinterpret_cast<__nv_bfloat162*>(dst + v) = __floats2bfloat162_rn(0.f, 0.f);
-    return;
-  }
-  const long long N = static_cast<long long>(prefix[a.batch]) * Hkv;
-  const long long s0 = static_cast<long long>(prefix[b]) * Hkv + static_cast<long long>(kvh) * nblk;
-  const long long s1 = s0 + nblk;
-  auto owner = [&](long long x) { return static_cast<int>(((x + 1) * P - 1) / N); };
-  auto start = [&](int cc) { return cc * N / P; };
-  const int c0 = owner(s0), c1 = owner(s1 - 1);
-  if (c0 == c1) return;  // written by the CTA that held the whole segment
-  float M = -INFINITY;
-  for (int cc = c0; cc <= c1; ++cc) {
-    if (cc > c0 && start(cc) == start(cc + 1)) continue;  // empty range
-    const long long slot = cc == c0 ? 2LL * cc + 1 : 2LL * cc;
-    M = fmaxf(M, a.part_ml[(slot * 8 + g) * 2]);
-  }
-  float l = 0.f, acc[V];
-#pragma unroll
-  for (int v = 0; v < V; ++v) acc[v] = 0.f;
-  for (int cc = c0; cc <= c1; ++cc) {
-    if (cc > c0 && start(cc) == start(cc + 1)) continue;
-    const long long slot = cc == c0 ? 2LL * cc + 1 : 2LL * cc;
-    const float f = fast_exp2(a.part_ml[(slot * 8 + g) * 2] - M);
-    l += f * a.part_ml[(slot * 8 + g) * 2 + 1];
-    const float* src = a.part_o + (slot * 8 + g) * D + lane * V;
-#pragma unroll
-    for (int v = 0; v < V; ++v) acc[v] += f * src[v];
-  }
-  const float inv = l > 0.f ? 1.f / l : 0.f;
-#pragma unroll
-  for (int v = 0; v < V; v += 2)
-    *reinterpret_cast<__nv_bfloat162*>(dst + v) = __floats2bfloat162_rn(acc[v] * inv, acc[v + 1] * inv);
 }
 
 // ============================================================ grid-split path
@@ -744,10 +931,16 @@ __global__ void __launch_bounds__(128) decode_split_merge_kernel(const DecodeArg
 }
 
 // ============================================================ host side
-constexpr int kWarps = 4;
-// Shared-memory budget of one CTA's stage rings: 64 KB lets two CTAs share an
-// SM next to the merge buffers and the prefix sums.
-constexpr int kStageBudget = 64 * 1024;
+#ifndef PA_DECODE_WARPS
+#define PA_DECODE_WARPS 4
+#endif
+#ifndef PA_DECODE_STAGE_KB
+#define PA_DECODE_STAGE_KB 64
+#endif
+constexpr int kWarps = PA_DECODE_WARPS;
+// Shared-memory budget of one CTA's stage rings (the CTA count per SM follows
+// from it); each warp gets kStageBudget / (kWarps * stage) stages, 2 to 8.
+constexpr int kStageBudget = PA_DECODE_STAGE_KB * 1024;
 
 constexpr int stages_for(int stage_bytes) {
   return kStageBudget / (kWarps * stage_bytes) < 2 ? 2
@@ -765,14 +958,22 @@ struct Inst {
   static_assert(PC::kPrefixOff + 1024 + (kMaxPersistentBatch + 1) * 4 <= 227 * 1024,
                 "shared memory over the per-CTA limit");
 
-  static int ctas_per_sm(int batch) {
+  // Per device, once: allow the largest shared-memory size any batch needs
+  // and record how many CTAs of it fit on an SM (the persistent grid is that
+  // times the SM count, the same for every call on the device).
+  static int ctas_per_sm() {
+    static int cached[kMaxDevices] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 1;
+    if (cached[dev] > 0) return cached[dev];
     auto* k = decode_persistent_kernel<D, BS, kWarps, kStages, FP8>;
+    const int smem = PC::smem_bytes(kMaxPersistentBatch);
     int n = 0;
-    const int smem = PC::smem_bytes(batch);
     if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
         cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, kWarps * 32, smem) != cudaSuccess)
       return 1;
-    return std::max(1, n);
+    cached[dev] = std::max(1, n);
+    return cached[dev];
   }
 
   static cudaError_t launch(const DecodeArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
@@ -781,18 +982,31 @@ struct Inst {
     const long long rows = static_cast<long long>(a.batch) * a.num_heads;
     if (a.persistent_ctas > 0) {
       auto* k = decode_persistent_kernel<D, BS, kWarps, kStages, FP8>;
-      const int smem = PC::smem_bytes(a.batch);
-      e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-      if (e != cudaSuccess) return e;
-      k<<<a.persistent_ctas, kWarps * 32, smem, stream>>>(kmap, vmap, a);
-      if ((e = cudaGetLastError()) != cudaSuccess) return e;
-      decode_persistent_merge_kernel<D><<<static_cast<unsigned>((rows + 3) / 4), 128, 0, stream>>>(
-          a, a.persistent_ctas);
-      return cudaGetLastError();
+      (void)ctas_per_sm();  // makes sure the shared-memory attribute is set on this device
+      // programmatic dependent launch: the prologue may overlap the kernel
+      // before this one on the stream (the kernel waits before reading K/V)
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(a.persistent_ctas);
+      cfg.blockDim = dim3(kWarps * 32);
+      cfg.dynamicSmemBytes = PC::smem_bytes(a.batch);
+      cfg.stream = stream;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+      attr[0].val.programmaticStreamSerializationAllowed = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      return cudaLaunchKernelEx(&cfg, k, kmap, vmap, a);
     }
     auto* k = decode_split_kernel<D, BS, kWarps, kStages, FP8>;
-    e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSplitSmem);
-    if (e != cudaSuccess) return e;
+    static bool attr_set[kMaxDevices] = {};
+    int dev = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    if (!attr_set[dev]) {
+      e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSplitSmem);
+      if (e != cudaSuccess) return e;
+      attr_set[dev] = true;
+    }
     dim3 grid(a.num_kv_heads, a.batch, a.num_splits);
     k<<<grid, kWarps * 32, kSplitSmem, stream>>>(kmap, vmap, a);
     if ((e = cudaGetLastError()) != cudaSuccess || a.num_splits <= 1) return e;
@@ -830,12 +1044,16 @@ DecodePlan plan_decode(int batch, int num_heads, int num_kv_heads, int head_dim,
   const size_t slot_floats = static_cast<size_t>(8) * head_dim + 8 * 2;  // one partial slot
   if (batch <= kMaxPersistentBatch) {
     const int per_sm = dispatch(head_dim, block_size, fp8,
-                                [&](auto inst) { return decltype(inst)::ctas_per_sm(batch); });
+                                [&](auto inst) { return decltype(inst)::ctas_per_sm(); });
     p.persistent_ctas = per_sm * num_sms;
+    p.persistent_slots_per_cta = kWarps;
     p.blocks_per_split = 0;
     p.num_splits = 0;
-    p.workspace_bytes = 2 * static_cast<size_t>(p.persistent_ctas) * slot_floats * sizeof(float) +
-                        (static_cast<size_t>(batch) + 1) * sizeof(int) + 256;
+    // two partial slots per warp
+    p.workspace_bytes =
+        2 * static_cast<size_t>(p.persistent_ctas) * kWarps * slot_floats * sizeof(float) +
+        (static_cast<size_t>(batch) + 1) * sizeof(int) + 16 +
+        static_cast<size_t>(batch) * num_kv_heads * sizeof(unsigned long long) + 256;
     return p;
   }
   (void)num_heads;

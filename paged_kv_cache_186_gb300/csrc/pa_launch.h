@@ -41,7 +41,9 @@ struct DecodeArgs {
   void* out;                  // (B, H, D) bf16
   float* part_o;              // partial slots: (slots, 8, D) fp32
   float* part_ml;             // (slots, 8, 2) fp32: (max, sum) per head
-  int* prefix_out;            // persistent path: (B+1) block prefix sums for the merge
+  int* prefix_out;            // persistent path: (B+1) block prefix sums
+  unsigned long long* seg_counters;  // persistent path: (B*Hkv) arrival counters
+  uint32_t epoch;             // persistent path: tag of this call in seg_counters
   uint32_t* err;
   int batch, num_heads, num_kv_heads, group, head_dim, block_size;
   int max_blocks, num_blocks, len_cap;
@@ -55,6 +57,7 @@ struct DecodeArgs {
 // grid-split (blocks per split, number of splits, one slot per split).
 struct DecodePlan {
   int persistent_ctas;
+  int persistent_slots_per_cta;  // warps per CTA: each warp owns 2 partial slots
   int blocks_per_split;
   int num_splits;
   size_t workspace_bytes;

@@ -17,6 +17,7 @@ namespace {
 constexpr int kStoreWarps = 4;
 
 __global__ void __launch_bounds__(kStoreWarps * 32) store_kv_kernel(const StoreArgs a) {
+  grid_launch_dependents();  // a following decode/prefill may start its prologue
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * kStoreWarps + warp;
   if (t >= a.num_tokens) return;
