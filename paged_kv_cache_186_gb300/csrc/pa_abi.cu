@@ -312,12 +312,15 @@ pa_status pa_prefill_varlen(const void* q, const pa_kv_cache* cache, const int32
   if (group != 1 && group != 2 && group != 4 && group != 8 && group != 16)
     return PA_ERR_UNSUPPORTED;
   if (batch > 65535 || cache->num_kv_heads > 65535) return PA_ERR_UNSUPPORTED;
+
   if (!std::isfinite(scale) || !(scale > 0.f)) return PA_ERR_SHAPE;
   if (!aligned16(q) || !aligned16(out)) return PA_ERR_ALIGN;
   DeviceInfo* dev = nullptr;
   if ((st = device_info(&dev)) != PA_OK) return st;
   const int tpt = pa::prefill_tokens_per_tile(group);
   const int qbound = max_q_len > 0 ? std::min(max_q_len, total_q) : total_q;
+  // the grid's z extent is the number of query-tile pairs of the longest sequence
+  if ((static_cast<long long>(qbound) + 2 * tpt - 1) / (2 * tpt) > 65535) return PA_ERR_UNSUPPORTED;
   // Q viewed as (head_dim, num_heads, total_q); one box = the G heads of a kv
   // head for tpt consecutive tokens, 64 dims (128 bytes) wide.
   CUtensorMap qmap, kmap, vmap;

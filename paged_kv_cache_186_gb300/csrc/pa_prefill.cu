@@ -9,25 +9,29 @@
 //   out[i, h] = sum_j softmax_j(scale * q[i,h] . K[j, h/G]) V[j, h/G]
 //
 // How (GB300 design):
-//   * One CTA per (128-row query tile, kv head, sequence). The 128 rows are
-//     128/G tokens x the G query heads of one kv head (GQA packing), so every
-//     K/V tile is loaded once for the whole head group.
-//   * Warp 0 streams the tile's Q once and then K and V tiles of 128 keys
-//     (128/bs physical blocks, one 3-D TMA box per block and 64-dim half,
-//     128B-swizzled), resolving logical -> physical blocks through the block
-//     table; blocks past the last needed key are fetched out of bounds so TMA
-//     fills them with zeros.
-//   * Warp 1 issues the tensor-core MMAs (tcgen05, fp32 accumulation in TMEM):
-//     S = Q K^T (M=128, N=128, K=128, operands from shared memory) and
-//     O += P V (A = P from TMEM, B = V from shared memory, MN-major).
-//   * Warps 2-5 own one TMEM lane (= one query row) each: read S, apply the
-//     bottom-right mask only on tiles that reach past the row's last visible
-//     key, run the online softmax in base 2 (the running max is only raised,
-//     and O rescaled, when it grows by more than 2^8, which keeps P <= 256
-//     and leaves O/l unchanged), write P as bf16 into the S columns, and in
-//     the end normalise O and store bf16 rows.
-//   * TMEM: 256 columns per CTA (S/P 128, O 128), two CTAs per SM.
+//   * A query tile is 128 rows = 128/G tokens x the G query heads of one kv
+//     head (GQA packing: every K/V tile serves the whole head group). One CTA
+//     per SM holds TWO consecutive query tiles of a (sequence, kv head) and
+//     walks the K/V tiles (128 keys) they need.
+//   * Warp 0 streams the two Q tiles once and K/V tiles through a 2-stage ring
+//     (128/bs physical blocks per tile, one 3-D TMA box per block and 64-dim
+//     half, 128B-swizzled), resolving logical -> physical blocks through the
+//     block table; blocks past the last needed key are fetched out of bounds
+//     so TMA fills them with zeros.
+//   * Warp 1 issues the tensor-core MMAs (tcgen05, fp32 accumulation in TMEM)
+//     in the order S0 = Q0 K^T, S1 = Q1 K^T, O0 += P0 V, O1 += P1 V for each
+//     K/V tile: while one softmax warpgroup works on its tile, the tensor core
+//     is busy with the other one's.
+//   * Warps 2-5 (tile 0) and 6-9 (tile 1) own one TMEM lane (= query row)
+//     each: read the S row, apply the bottom-right mask only on tiles that
+//     reach past the row's last visible key, run the online softmax in base 2
+//     (the running max is only raised, and O rescaled, when it grows by more
+//     than 2^8, which keeps P <= 256 and leaves O/l unchanged), write P as
+//     bf16 into the S columns, and at the end normalise O and store bf16 rows.
+//   * TMEM: 512 columns (S0, S1, O0, O1, 128 each); shared memory: Q0, Q1 and
+//     two K and two V stages (192 KB).
 #include <algorithm>
+#include <type_traits>
 
 #include "pa_device.cuh"
 #include "pa_prefill.h"
@@ -37,17 +41,30 @@ namespace pa {
 
 namespace {
 
-constexpr int kBM = 128;       // query rows per tile
-constexpr int kBN = 128;       // keys per tile
-constexpr int kD = 128;        // head_dim
-constexpr int kSub = 128 * kBM;  // bytes of one 64-dim (128-byte-wide) half of a 128-row tile
-constexpr int kTileBytes = 2 * kSub;  // 32 KB
-constexpr int kSmem = 1024 + 3 * kTileBytes;
-constexpr int kThreads = 192;
-constexpr uint32_t kTmemCols = 256;
+constexpr int kBM = 128;               // query rows per tile
+constexpr int kBN = 128;               // keys per tile
+constexpr int kD = 128;                // head_dim
+constexpr int kSub = 128 * kBM;        // bytes of one 64-dim (128-byte-wide) half of a 128-row tile
+constexpr int kTileBytes = 2 * kSub;   // 32 KB
+constexpr int kStages = 2;             // K/V ring depth
+constexpr int kSmem = 1024 + (2 + 2 * kStages) * kTileBytes;
+constexpr int kThreads = 320;          // producer, MMA, 2 x 4 softmax warps
+constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
-enum { BAR_Q = 0, BAR_KF, BAR_VF, BAR_KE, BAR_VE, BAR_S, BAR_P, BAR_O, BAR_DRAIN, NBAR };
+// barrier indices
+enum {
+  BAR_Q = 0,
+  BAR_KF = 1,   // + stage
+  BAR_KE = 3,   // + stage
+  BAR_VF = 5,   // + stage
+  BAR_VE = 7,   // + stage
+  BAR_S = 9,    // + tile
+  BAR_P = 11,   // + tile
+  BAR_O = 13,   // + tile
+  BAR_DRAIN = 15,
+  NBAR = 16
+};
 
 // Bounded wait that also gives up when another role of the CTA has aborted.
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity,
@@ -74,7 +91,7 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
 }
 
 template <int BS>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap qmap,
                    const __grid_constant__ CUtensorMap kmap,
                    const __grid_constant__ CUtensorMap vmap, const PrefillArgs a) {
@@ -84,27 +101,38 @@ __global__ void __launch_bounds__(kThreads, 2)
   __shared__ uint32_t tmem_slot;
   __shared__ volatile int abort_flag;
 
+  // launched as a programmatic dependent of the store that wrote the new
+  // tokens' K/V: wait for it before reading anything
+  grid_dependency_wait();
+
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int b = blockIdx.z, kvh = blockIdx.y;
-  const int qt = a.num_qtiles - 1 - static_cast<int>(blockIdx.x);  // heaviest tiles first
+  // grid (kv head, sequence, tile pair): CTAs are dispatched x fastest, so the
+  // last tile pairs of every sequence (the most keys) start first
+  const int kvh = blockIdx.x, b = blockIdx.y;
+  const int npairs = (a.num_qtiles + 1) / 2;
+  const int pair = npairs - 1 - static_cast<int>(blockIdx.z);
   const int G = a.group, TPT = a.tokens_per_tile;
 
   const int q0 = a.cu_q[b];
   const int q_len = max(a.cu_q[b + 1] - q0, 0);
   const int kv_len = max(a.cu_k[b + 1] - a.cu_k[b], 0);
   const int cached = max(kv_len - q_len, 0);
-  const int t0 = qt * TPT;
-  if (t0 >= q_len) return;
-  const int t_end = min(t0 + TPT, q_len);
-  const int n_keys = min(cached + t_end, kv_len);  // keys the tile's last row can see
-  const int T = (n_keys + kBN - 1) / kBN;
+  const int t00 = 2 * pair * TPT;  // first token of query tile 0
+  if (t00 >= q_len) return;
+  const bool has1 = t00 + TPT < q_len;
+  // K/V tiles each query tile needs (keys its last row can see)
+  int Tq[2];
+  Tq[0] = (min(cached + min(t00 + TPT, q_len), kv_len) + kBN - 1) / kBN;
+  Tq[1] = has1 ? (min(cached + min(t00 + 2 * TPT, q_len), kv_len) + kBN - 1) / kBN : 0;
+  const int T = max(Tq[0], Tq[1]);
   __nv_bfloat16* const out = static_cast<__nv_bfloat16*>(a.out);
   const int H = a.num_heads;
 
   if (T == 0) {  // no keys at all (invalid q_len > kv_len = 0): zero rows
-    for (int e = threadIdx.x; e < (t_end - t0) * G * (kD / 8); e += kThreads) {
+    const int rows = (min(t00 + 2 * TPT, q_len) - t00) * G;
+    for (int e = threadIdx.x; e < rows * (kD / 8); e += kThreads) {
       const int row = e / (kD / 8), c = e % (kD / 8);
-      const int tok = t0 + row / G, g = row % G;
+      const int tok = t00 + row / G, g = row % G;
       reinterpret_cast<uint4*>(out + (static_cast<long long>(q0 + tok) * H + kvh * G + g) * kD)[c] =
           make_uint4(0, 0, 0, 0);
     }
@@ -114,12 +142,14 @@ __global__ void __launch_bounds__(kThreads, 2)
   const uint32_t raw = smem_addr(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* const base_ptr = smem_raw + (base - raw);
-  const uint32_t q_s = base, k_s = base + kTileBytes, v_s = base + 2 * kTileBytes;
+  auto q_s = [&](int i) { return base + i * kTileBytes; };
+  auto k_s = [&](int s) { return base + (2 + s) * kTileBytes; };
+  auto v_s = [&](int s) { return base + (2 + kStages + s) * kTileBytes; };
   const uint32_t bar0 = smem_addr(&bars[0]);
   auto bar = [&](int i) { return bar0 + 8u * i; };
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < NBAR; ++i) mbar_init(bar(i), i == BAR_P ? 4 : 1);
+    for (int i = 0; i < NBAR; ++i) mbar_init(bar(i), (i == BAR_P || i == BAR_P + 1) ? 4 : 1);
     abort_flag = 0;
     fence_barrier_init();
     fence_proxy_async_smem();
@@ -132,19 +162,24 @@ __global__ void __launch_bounds__(kThreads, 2)
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = tmem_slot;
-  const uint32_t tS = tmem, tO = tmem + 128;  // columns; P overwrites S's first 64 columns
+  auto tS = [&](int i) { return tmem + 128u * i; };        // S_i, P_i in its first 64 columns
+  auto tO = [&](int i) { return tmem + 256u + 128u * i; };  // O_i
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     int k_issued = 0, v_issued = 0;
     if (lane == 0) {
-      mbar_arrive_expect_tx(bar(BAR_Q), kTileBytes);
-      tma_load_3d(q_s, &qmap, bar(BAR_Q), 0, kvh * G, q0 + t0);
-      tma_load_3d(q_s + kSub, &qmap, bar(BAR_Q), 64, kvh * G, q0 + t0);
+      mbar_arrive_expect_tx(bar(BAR_Q), (has1 ? 2 : 1) * kTileBytes);
+      for (int i = 0; i < (has1 ? 2 : 1); ++i) {
+        tma_load_3d(q_s(i), &qmap, bar(BAR_Q), 0, kvh * G, q0 + t00 + i * TPT);
+        tma_load_3d(q_s(i) + kSub, &qmap, bar(BAR_Q), 64, kvh * G, q0 + t00 + i * TPT);
+      }
     }
     const long long bt_row = static_cast<long long>(b) * a.max_blocks;
+    const int n_keys = min(cached + min(t00 + 2 * TPT, q_len), kv_len);
     const int oob = a.num_blocks * BS;  // first row past the pool: TMA fills zeros
     for (int n = 0; n < T; ++n) {
+      const int s = n % kStages;
       int rc = oob;
       if (lane < kBlocksPerTile) {
         const int lb = n * kBlocksPerTile + lane;
@@ -157,33 +192,39 @@ __global__ void __launch_bounds__(kThreads, 2)
           }
         }
       }
-      if (n > 0 && !warp_wait(bar(BAR_KE), (n - 1) & 1, &abort_flag, a.err)) break;
-      if (lane == 0) mbar_arrive_expect_tx(bar(BAR_KF), kTileBytes);
+      if (n >= kStages &&
+          !warp_wait(bar(BAR_KE + s), ((n - kStages) / kStages) & 1, &abort_flag, a.err))
+        break;
+      if (lane == 0) mbar_arrive_expect_tx(bar(BAR_KF + s), kTileBytes);
 #pragma unroll
       for (int i = 0; i < kBlocksPerTile; ++i) {
         const int c = __shfl_sync(0xffffffffu, rc, i);
         if (lane == 0) {
-          tma_load_3d(k_s + i * BS * 128, &kmap, bar(BAR_KF), 0, kvh, c);
-          tma_load_3d(k_s + kSub + i * BS * 128, &kmap, bar(BAR_KF), 64, kvh, c);
+          tma_load_3d(k_s(s) + i * BS * 128, &kmap, bar(BAR_KF + s), 0, kvh, c);
+          tma_load_3d(k_s(s) + kSub + i * BS * 128, &kmap, bar(BAR_KF + s), 64, kvh, c);
         }
       }
       ++k_issued;
-      if (n > 0 && !warp_wait(bar(BAR_VE), (n - 1) & 1, &abort_flag, a.err)) break;
-      if (lane == 0) mbar_arrive_expect_tx(bar(BAR_VF), kTileBytes);
+      if (n >= kStages &&
+          !warp_wait(bar(BAR_VE + s), ((n - kStages) / kStages) & 1, &abort_flag, a.err))
+        break;
+      if (lane == 0) mbar_arrive_expect_tx(bar(BAR_VF + s), kTileBytes);
 #pragma unroll
       for (int i = 0; i < kBlocksPerTile; ++i) {
         const int c = __shfl_sync(0xffffffffu, rc, i);
         if (lane == 0) {
-          tma_load_3d(v_s + i * BS * 128, &vmap, bar(BAR_VF), 0, kvh, c);
-          tma_load_3d(v_s + kSub + i * BS * 128, &vmap, bar(BAR_VF), 64, kvh, c);
+          tma_load_3d(v_s(s) + i * BS * 128, &vmap, bar(BAR_VF + s), 0, kvh, c);
+          tma_load_3d(v_s(s) + kSub + i * BS * 128, &vmap, bar(BAR_VF + s), 64, kvh, c);
         }
       }
       ++v_issued;
     }
     if (abort_flag) {
       // let the copies already in flight land before shared memory is released
-      if (k_issued > 0) (void)mbar_wait(bar(BAR_KF), (k_issued - 1) & 1);
-      if (v_issued > 0) (void)mbar_wait(bar(BAR_VF), (v_issued - 1) & 1);
+      for (int n = max(0, k_issued - kStages); n < k_issued; ++n)
+        (void)mbar_wait(bar(BAR_KF + n % kStages), (n / kStages) & 1);
+      for (int n = max(0, v_issued - kStages); n < v_issued; ++n)
+        (void)mbar_wait(bar(BAR_VF + n % kStages), (n / kStages) & 1);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issue
@@ -191,44 +232,64 @@ __global__ void __launch_bounds__(kThreads, 2)
     constexpr uint32_t kIdescPV = tc::idesc_bf16_f32(kBM, kD, false, true);
     bool ok = warp_wait(bar(BAR_Q), 0, &abort_flag, a.err);
     for (int n = 0; ok && n < T; ++n) {
-      if (!warp_wait(bar(BAR_KF), n & 1, &abort_flag, a.err)) break;
-      if (n > 0 && !warp_wait(bar(BAR_O), (n - 1) & 1, &abort_flag, a.err)) break;
-      tc::fence_after_sync();
-      if (lane == 0) {
-#pragma unroll
-        for (int kk = 0; kk < kD / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kSub + (kk & 3) * 32;
-          tc::mma_ss(tS, tc::smem_desc_sw128(q_s + off, 16, 1024),
-                     tc::smem_desc_sw128(k_s + off, 16, 1024), kIdescQK, kk > 0 ? 1u : 0u);
+      const int s = n % kStages;
+      const uint32_t par = (n / kStages) & 1;
+      if (!warp_wait(bar(BAR_KF + s), par, &abort_flag, a.err)) break;
+      for (int i = 0; i < 2; ++i) {
+        if (n >= Tq[i]) continue;
+        // S_i / P_i columns are free once O_i += P_i V of the previous tile is done
+        if (n > 0 && !warp_wait(bar(BAR_O + i), (n - 1) & 1, &abort_flag, a.err)) {
+          ok = false;
+          break;
         }
-        tc::commit(bar(BAR_S));
-        tc::commit(bar(BAR_KE));
+        tc::fence_after_sync();
+        if (lane == 0) {
+#pragma unroll
+          for (int kk = 0; kk < kD / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * kSub + (kk & 3) * 32;
+            tc::mma_ss(tS(i), tc::smem_desc_sw128(q_s(i) + off, 16, 1024),
+                       tc::smem_desc_sw128(k_s(s) + off, 16, 1024), kIdescQK, kk > 0 ? 1u : 0u);
+          }
+          tc::commit(bar(BAR_S + i));
+        }
+        __syncwarp();
       }
+      if (!ok) break;
+      if (lane == 0) tc::commit(bar(BAR_KE + s));
       __syncwarp();
-      if (!warp_wait(bar(BAR_P), n & 1, &abort_flag, a.err)) break;
-      if (!warp_wait(bar(BAR_VF), n & 1, &abort_flag, a.err)) break;
+      if (!warp_wait(bar(BAR_VF + s), par, &abort_flag, a.err)) break;
       // rows of the last, partly filled physical block past kv_len hold
       // whatever the pool had there: zero them so that P = 0 times V stays 0
       const int r0 = kv_len - n * kBN;
       if (r0 > 0 && r0 < kBN && (r0 % BS) != 0) {
         const int r1 = min(kBN, (r0 / BS + 1) * BS);
+        uint8_t* vp = base_ptr + (v_s(s) - base);
         for (int e = lane; e < (r1 - r0) * 16; e += 32) {
           const int row = r0 + (e >> 4), c = e & 15;
-          *reinterpret_cast<uint4*>(base_ptr + 2 * kTileBytes + (c >> 3) * kSub + row * 128 +
-                                    (c & 7) * 16) = make_uint4(0, 0, 0, 0);
+          *reinterpret_cast<uint4*>(vp + (c >> 3) * kSub + row * 128 + (c & 7) * 16) =
+              make_uint4(0, 0, 0, 0);
         }
         fence_proxy_async_smem();
         __syncwarp();
       }
-      tc::fence_after_sync();
-      if (lane == 0) {
+      for (int i = 0; i < 2; ++i) {
+        if (n >= Tq[i]) continue;
+        if (!warp_wait(bar(BAR_P + i), n & 1, &abort_flag, a.err)) {
+          ok = false;
+          break;
+        }
+        tc::fence_after_sync();
+        if (lane == 0) {
 #pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk)
-          tc::mma_ts(tO, tS + kk * 8, tc::smem_desc_sw128(v_s + kk * 16 * 128, kSub, 1024),
-                     kIdescPV, (n > 0 || kk > 0) ? 1u : 0u);
-        tc::commit(bar(BAR_O));
-        tc::commit(bar(BAR_VE));
+          for (int kk = 0; kk < kBN / 16; ++kk)
+            tc::mma_ts(tO(i), tS(i) + kk * 8, tc::smem_desc_sw128(v_s(s) + kk * 16 * 128, kSub, 1024),
+                       kIdescPV, (n > 0 || kk > 0) ? 1u : 0u);
+          tc::commit(bar(BAR_O + i));
+        }
+        __syncwarp();
       }
+      if (!ok) break;
+      if (lane == 0) tc::commit(bar(BAR_VE + s));
       __syncwarp();
     }
     if (abort_flag) {  // make sure no MMA is still running before TMEM is freed
@@ -238,101 +299,126 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
   } else {
     // ------------------------------------------------------------ softmax
-    const int wq = warp & 3;
+    const int ti = (warp - 2) / 4;  // query tile of this warpgroup
+    const int Tn = Tq[ti];
+    const int wq = warp & 3;        // TMEM lane quarter this warp may access
     const int r = 32 * wq + lane;
-    const int tok = t0 + r / G, g = r % G;
-    const bool row_valid = tok < t_end;
+    const int tok = t00 + ti * TPT + r / G, g = r % G;
+    const bool row_valid = tok < q_len;
     const int last_key = min(min(tok, q_len - 1) + cached, kv_len - 1);  // last visible key
     const uint32_t trow = static_cast<uint32_t>(32 * wq) << 16;
     const float sl2 = a.scale_log2;
     float m_used = -INFINITY, l = 0.f;
     bool ok = true;
-    for (int n = 0; n < T; ++n) {
-      if (!warp_wait(bar(BAR_S), n & 1, &abort_flag, a.err)) {
+    for (int n = 0; n < Tn; ++n) {
+      if (!warp_wait(bar(BAR_S + ti), n & 1, &abort_flag, a.err)) {
         ok = false;
         break;
       }
       tc::fence_after_sync();
       const int lim = last_key - n * kBN;  // keys 0..lim of this tile are visible
-      uint32_t u[32];
+      // most tiles lie wholly left of every row's diagonal: no mask there
+      const bool full = __all_sync(0xffffffffu, lim >= kBN - 1);
       float mx = -INFINITY;
+      auto row_max = [&](auto masked) {
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        tc::tmem_ld32(tS + trow + 32 * c, u);
-        tc::tmem_wait_ld();
+        for (int c = 0; c < 4; c += 2) {
+          uint32_t u0[32], u1[32];
+          tc::tmem_ld32(tS(ti) + trow + 32 * c, u0);
+          tc::tmem_ld32(tS(ti) + trow + 32 * c + 32, u1);
+          tc::tmem_wait_ld();
 #pragma unroll
-        for (int j = 0; j < 32; ++j)
-          mx = fmaxf(mx, (32 * c + j <= lim) ? __uint_as_float(u[j]) : -INFINITY);
-      }
+          for (int j = 0; j < 32; ++j) {
+            if constexpr (decltype(masked)::value) {
+              mx = fmaxf(mx, (32 * c + j <= lim) ? __uint_as_float(u0[j]) : -INFINITY);
+              mx = fmaxf(mx, (32 * c + 32 + j <= lim) ? __uint_as_float(u1[j]) : -INFINITY);
+            } else {
+              mx = fmaxf(mx, fmaxf(__uint_as_float(u0[j]), __uint_as_float(u1[j])));
+            }
+          }
+        }
+      };
+      if (full) row_max(std::false_type{}); else row_max(std::true_type{});
       const float m_tile = mx * sl2;
       if (n == 0) {
         m_used = m_tile;
       } else if (__any_sync(0xffffffffu, m_tile > m_used + kRescaleThreshold)) {
-        if (!warp_wait(bar(BAR_O), (n - 1) & 1, &abort_flag, a.err)) {
+        if (!warp_wait(bar(BAR_O + ti), (n - 1) & 1, &abort_flag, a.err)) {
           ok = false;
           break;
         }
         tc::fence_after_sync();
         const float m_new = fmaxf(m_used, m_tile);
         const float alpha = fast_exp2(m_used - m_new);
+        uint32_t w[32];
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-          tc::tmem_ld32(tO + trow + 32 * c, u);
+          tc::tmem_ld32(tO(ti) + trow + 32 * c, w);
           tc::tmem_wait_ld();
 #pragma unroll
-          for (int j = 0; j < 32; ++j) u[j] = __float_as_uint(__uint_as_float(u[j]) * alpha);
-          tc::tmem_st32(tO + trow + 32 * c, u);
+          for (int j = 0; j < 32; ++j) w[j] = __float_as_uint(__uint_as_float(w[j]) * alpha);
+          tc::tmem_st32(tO(ti) + trow + 32 * c, w);
         }
         tc::tmem_wait_st();
         l *= alpha;
         m_used = m_new;
       }
       // P = 2^(s*scale*log2e - m_used) as bf16, keys 64h..64h+63 -> columns 32h..32h+31
+      // (columns 32h.. are read before they are overwritten); pairs of keys
+      // share one packed FMA for the exponent argument and one packed add
+      const uint64_t sl2x2 = tc::f32x2(sl2, sl2), nmx2 = tc::f32x2(-m_used, -m_used);
+      uint64_t lsum = tc::f32x2(0.f, 0.f);
+      auto probs = [&](auto masked) {
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint32_t u0[32], u1[32], w[32];
-        tc::tmem_ld32(tS + trow + 64 * h, u0);
-        tc::tmem_ld32(tS + trow + 64 * h + 32, u1);
-        tc::tmem_wait_ld();
+        for (int h = 0; h < 2; ++h) {
+          uint32_t u[2][32], w[32];
+          tc::tmem_ld32(tS(ti) + trow + 64 * h, u[0]);
+          tc::tmem_ld32(tS(ti) + trow + 64 * h + 32, u[1]);
+          tc::tmem_wait_ld();
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const int k0 = 64 * h + 2 * j;
-          const float p0 = k0 <= lim ? fast_exp2(fmaf(__uint_as_float(u0[2 * j]), sl2, -m_used)) : 0.f;
-          const float p1 =
-              k0 + 1 <= lim ? fast_exp2(fmaf(__uint_as_float(u0[2 * j + 1]), sl2, -m_used)) : 0.f;
-          l += p0 + p1;
-          w[j] = pack_bf16x2(p0, p1);
+          for (int j = 0; j < 32; ++j) {
+            const int c = j >> 4, e = 2 * (j & 15);
+            const uint64_t xa = tc::fma_f32x2(
+                tc::f32x2(__uint_as_float(u[c][e]), __uint_as_float(u[c][e + 1])), sl2x2, nmx2);
+            float x0, x1;
+            tc::f32x2_split(xa, x0, x1);
+            float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
+            if constexpr (decltype(masked)::value) {
+              const int k0 = 64 * h + 32 * c + e;
+              p0 = k0 <= lim ? p0 : 0.f;
+              p1 = k0 + 1 <= lim ? p1 : 0.f;
+            }
+            lsum = tc::add_f32x2(lsum, tc::f32x2(p0, p1));
+            w[j] = pack_bf16x2(p0, p1);
+          }
+          tc::tmem_st32(tS(ti) + trow + 32 * h, w);
         }
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const int k0 = 64 * h + 32 + 2 * j;
-          const float p0 = k0 <= lim ? fast_exp2(fmaf(__uint_as_float(u1[2 * j]), sl2, -m_used)) : 0.f;
-          const float p1 =
-              k0 + 1 <= lim ? fast_exp2(fmaf(__uint_as_float(u1[2 * j + 1]), sl2, -m_used)) : 0.f;
-          l += p0 + p1;
-          w[16 + j] = pack_bf16x2(p0, p1);
-        }
-        tc::tmem_st32(tS + trow + 32 * h, w);
+      };
+      if (full) probs(std::false_type{}); else probs(std::true_type{});
+      {
+        float la, lb;
+        tc::f32x2_split(lsum, la, lb);
+        l += la + lb;
       }
       tc::tmem_wait_st();
       tc::fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(BAR_P));
+      if (lane == 0) mbar_arrive(bar(BAR_P + ti));
     }
-    if (ok && warp_wait(bar(BAR_O), (T - 1) & 1, &abort_flag, a.err)) {
+    if (ok && Tn > 0 && warp_wait(bar(BAR_O + ti), (Tn - 1) & 1, &abort_flag, a.err)) {
       tc::fence_after_sync();
       const float inv = l > 0.f ? 1.f / l : 0.f;
       __nv_bfloat16* orow = out + (static_cast<long long>(q0 + tok) * H + kvh * G + g) * kD;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        uint32_t u[32];
-        tc::tmem_ld32(tO + trow + 32 * c, u);
+        uint32_t w[32];
+        tc::tmem_ld32(tO(ti) + trow + 32 * c, w);
         tc::tmem_wait_ld();
         if (row_valid) {
           uint32_t pk[16];
 #pragma unroll
           for (int j = 0; j < 16; ++j)
-            pk[j] = pack_bf16x2(__uint_as_float(u[2 * j]) * inv, __uint_as_float(u[2 * j + 1]) * inv);
+            pk[j] = pack_bf16x2(__uint_as_float(w[2 * j]) * inv, __uint_as_float(w[2 * j + 1]) * inv);
           uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c);
 #pragma unroll
           for (int j = 0; j < 4; ++j)
@@ -350,26 +436,41 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
 }
 
+template <int BS>
+cudaError_t launch_bs(const PrefillArgs& a, const CUtensorMap& qmap, const CUtensorMap& kmap,
+                      const CUtensorMap& vmap, cudaStream_t stream) {
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!attr_set[dev]) {
+    e = cudaFuncSetAttribute(prefill_kernel<BS>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  // programmatic dependent launch: may start while the preceding store runs
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.num_kv_heads, a.batch, (a.num_qtiles + 1) / 2);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, prefill_kernel<BS>, qmap, kmap, vmap, a);
+}
+
 }  // namespace
 
 cudaError_t launch_prefill(const PrefillArgs& a, const CUtensorMap& qmap, const CUtensorMap& kmap,
                            const CUtensorMap& vmap, cudaStream_t stream) {
   if (a.head_dim != kD || kBM % a.group != 0) return cudaErrorInvalidValue;
-  dim3 grid(a.num_qtiles, a.num_kv_heads, a.batch);
-  if (a.block_size == 16) {
-    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<16>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
-    if (e != cudaSuccess) return e;
-    prefill_kernel<16><<<grid, kThreads, kSmem, stream>>>(qmap, kmap, vmap, a);
-  } else if (a.block_size == 32) {
-    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<32>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
-    if (e != cudaSuccess) return e;
-    prefill_kernel<32><<<grid, kThreads, kSmem, stream>>>(qmap, kmap, vmap, a);
-  } else {
-    return cudaErrorInvalidValue;
-  }
-  return cudaGetLastError();
+  if (a.block_size == 16) return launch_bs<16>(a, qmap, kmap, vmap, stream);
+  if (a.block_size == 32) return launch_bs<32>(a, qmap, kmap, vmap, stream);
+  return cudaErrorInvalidValue;
 }
 
 int prefill_tokens_per_tile(int group) { return kBM / group; }
