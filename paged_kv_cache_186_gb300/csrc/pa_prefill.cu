@@ -106,17 +106,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   grid_dependency_wait();
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // grid (kv head, sequence, tile pair): CTAs are dispatched x fastest, so the
-  // last tile pairs of every sequence (the most keys) start first
+  // grid (kv head, sequence, tile pair counted from each sequence's end): CTAs
+  // are dispatched x fastest, so every sequence's last pair (its most keys)
+  // starts in the first wave
   const int kvh = blockIdx.x, b = blockIdx.y;
-  const int npairs = (a.num_qtiles + 1) / 2;
-  const int pair = npairs - 1 - static_cast<int>(blockIdx.z);
   const int G = a.group, TPT = a.tokens_per_tile;
 
   const int q0 = a.cu_q[b];
   const int q_len = max(a.cu_q[b + 1] - q0, 0);
   const int kv_len = max(a.cu_k[b + 1] - a.cu_k[b], 0);
   const int cached = max(kv_len - q_len, 0);
+  const int pair = (q_len + 2 * TPT - 1) / (2 * TPT) - 1 - static_cast<int>(blockIdx.z);
+  if (pair < 0) return;
   const int t00 = 2 * pair * TPT;  // first token of query tile 0
   if (t00 >= q_len) return;
   const bool has1 = t00 + TPT < q_len;
