@@ -48,7 +48,14 @@ constexpr int kSub = 128 * kBM;        // bytes of one 64-dim (128-byte-wide) ha
 constexpr int kTileBytes = 2 * kSub;   // 32 KB
 constexpr int kStages = 2;             // K/V ring depth
 constexpr int kSmem = 1024 + (2 + 2 * kStages) * kTileBytes;
-constexpr int kThreads = 320;          // producer, MMA, 2 x 4 softmax warps
+constexpr int kThreads = 384;          // 2 x 4 softmax warps, then producer, MMA, 2 idle
+// Register split (setmaxnreg): launched at 65536/384 -> 168 per thread; the
+// producer/MMA warpgroup drops to 56 so the two softmax warpgroups can hold a
+// whole 128-key score row: 2*128*224 + 128*56 = 384*168.
+constexpr int kSoftmaxRegs = 224;
+constexpr int kControlRegs = 56;
+static_assert(2 * 128 * kSoftmaxRegs + 128 * kControlRegs <= kThreads * 168,
+              "register split exceeds the launch allocation");
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
@@ -155,7 +162,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_barrier_init();
     fence_proxy_async_smem();
   }
-  if (warp == 1) {
+  if (warp == 9) {
     tc::tmem_alloc(smem_addr(&tmem_slot), kTmemCols);
     tc::tmem_relinquish();
   }
@@ -166,7 +173,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto tS = [&](int i) { return tmem + 128u * i; };        // S_i, P_i in its first 64 columns
   auto tO = [&](int i) { return tmem + 256u + 128u * i; };  // O_i
 
-  if (warp == 0) {
+  if (warp >= 8) {
+   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kControlRegs));
+   if (warp == 8) {
     // ------------------------------------------------------------ producer
     int k_issued = 0, v_issued = 0;
     if (lane == 0) {
@@ -227,7 +236,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int n = max(0, v_issued - kStages); n < v_issued; ++n)
         (void)mbar_wait(bar(BAR_VF + n % kStages), (n / kStages) & 1);
     }
-  } else if (warp == 1) {
+  } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issue
     constexpr uint32_t kIdescQK = tc::idesc_bf16_f32(kBM, kBN, false, false);
     constexpr uint32_t kIdescPV = tc::idesc_bf16_f32(kBM, kD, false, true);
@@ -298,9 +307,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       (void)mbar_wait(bar(BAR_DRAIN), 0);
     }
+   }
   } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kSoftmaxRegs));
     // ------------------------------------------------------------ softmax
-    const int ti = (warp - 2) / 4;  // query tile of this warpgroup
+    const int ti = warp / 4;        // query tile of this warpgroup
     const int Tn = Tq[ti];
     const int wq = warp & 3;        // TMEM lane quarter this warp may access
     const int r = 32 * wq + lane;
@@ -318,28 +329,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc::fence_after_sync();
       const int lim = last_key - n * kBN;  // keys 0..lim of this tile are visible
+      // the whole score row in registers: one TMEM round trip
+      uint32_t u[4][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tc::tmem_ld32(tS(ti) + trow + 32 * c, u[c]);
+      tc::tmem_wait_ld();
       // most tiles lie wholly left of every row's diagonal: no mask there
-      const bool full = __all_sync(0xffffffffu, lim >= kBN - 1);
+      if (!__all_sync(0xffffffffu, lim >= kBN - 1)) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (32 * c + j > lim) u[c][j] = __float_as_uint(-INFINITY);
+      }
       float mx = -INFINITY;
-      auto row_max = [&](auto masked) {
 #pragma unroll
-        for (int c = 0; c < 4; c += 2) {
-          uint32_t u0[32], u1[32];
-          tc::tmem_ld32(tS(ti) + trow + 32 * c, u0);
-          tc::tmem_ld32(tS(ti) + trow + 32 * c + 32, u1);
-          tc::tmem_wait_ld();
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            if constexpr (decltype(masked)::value) {
-              mx = fmaxf(mx, (32 * c + j <= lim) ? __uint_as_float(u0[j]) : -INFINITY);
-              mx = fmaxf(mx, (32 * c + 32 + j <= lim) ? __uint_as_float(u1[j]) : -INFINITY);
-            } else {
-              mx = fmaxf(mx, fmaxf(__uint_as_float(u0[j]), __uint_as_float(u1[j])));
-            }
-          }
-        }
-      };
-      if (full) row_max(std::false_type{}); else row_max(std::true_type{});
+      for (int j = 0; j < 32; ++j)
+        mx = fmaxf(mx, fmaxf(fmaxf(__uint_as_float(u[0][j]), __uint_as_float(u[1][j])),
+                             fmaxf(__uint_as_float(u[2][j]), __uint_as_float(u[3][j]))));
       const float m_tile = mx * sl2;
       if (n == 0) {
         m_used = m_tile;
@@ -365,37 +372,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         m_used = m_new;
       }
       // P = 2^(s*scale*log2e - m_used) as bf16, keys 64h..64h+63 -> columns 32h..32h+31
-      // (columns 32h.. are read before they are overwritten); pairs of keys
-      // share one packed FMA for the exponent argument and one packed add
+      // (masked keys hold -inf: P = 0); pairs of keys share one packed FMA for
+      // the exponent argument and one packed add for the row sum
       const uint64_t sl2x2 = tc::f32x2(sl2, sl2), nmx2 = tc::f32x2(-m_used, -m_used);
       uint64_t lsum = tc::f32x2(0.f, 0.f);
-      auto probs = [&](auto masked) {
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          uint32_t u[2][32], w[32];
-          tc::tmem_ld32(tS(ti) + trow + 64 * h, u[0]);
-          tc::tmem_ld32(tS(ti) + trow + 64 * h + 32, u[1]);
-          tc::tmem_wait_ld();
+      for (int h = 0; h < 2; ++h) {
+        uint32_t w[32];
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const int c = j >> 4, e = 2 * (j & 15);
-            const uint64_t xa = tc::fma_f32x2(
-                tc::f32x2(__uint_as_float(u[c][e]), __uint_as_float(u[c][e + 1])), sl2x2, nmx2);
-            float x0, x1;
-            tc::f32x2_split(xa, x0, x1);
-            float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
-            if constexpr (decltype(masked)::value) {
-              const int k0 = 64 * h + 32 * c + e;
-              p0 = k0 <= lim ? p0 : 0.f;
-              p1 = k0 + 1 <= lim ? p1 : 0.f;
-            }
-            lsum = tc::add_f32x2(lsum, tc::f32x2(p0, p1));
-            w[j] = pack_bf16x2(p0, p1);
-          }
-          tc::tmem_st32(tS(ti) + trow + 32 * h, w);
+        for (int j = 0; j < 32; ++j) {
+          const int c = 2 * h + (j >> 4), e = 2 * (j & 15);
+          const uint64_t xa = tc::fma_f32x2(
+              tc::f32x2(__uint_as_float(u[c][e]), __uint_as_float(u[c][e + 1])), sl2x2, nmx2);
+          float x0, x1;
+          tc::f32x2_split(xa, x0, x1);
+          const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
+          lsum = tc::add_f32x2(lsum, tc::f32x2(p0, p1));
+          w[j] = pack_bf16x2(p0, p1);
         }
-      };
-      if (full) probs(std::false_type{}); else probs(std::true_type{});
+        tc::tmem_st32(tS(ti) + trow + 32 * h, w);
+      }
       {
         float la, lb;
         tc::f32x2_split(lsum, la, lb);
@@ -431,7 +427,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc::fence_before_sync();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == 9) {
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, kTmemCols);
   }
