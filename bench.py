@@ -84,7 +84,7 @@ def traffic_from_profile(kernel_file: str, workload: str):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on
     the current kernel source (the summary records the source's sha256)."""
     src = os.path.join(ROOT, "paged_kv_cache_186_gb300", "csrc", kernel_file)
-    prof = os.path.join(ROOT, "profiles", f"decode_split_kernel_{workload}.md")
+    prof = os.path.join(ROOT, "profiles", f"decode_persistent_kernel_{workload}.md")
     try:
         sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
         text = open(prof).read()
@@ -409,7 +409,8 @@ def run_gpu(args, world, rank, local):
     peak, peak_kind = peaks()
     achieved = step_bytes / (dec_avg_ms / 1e3) / 1e9
     traffic = traffic_from_profile("pa_decode.cu", name)
-    n_launch = 1 + 1 + (1 if ws_bytes > 0 else 0)
+    # store_kv + decode; the grid-split path (batches above 2048) adds a merge
+    n_launch = 2 if B <= 2048 else 3
     clocks = sampler.summary(t_wall0, t_wall1) if sampler else None
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
@@ -421,7 +422,7 @@ def run_gpu(args, world, rank, local):
                    "block_size": w["block_size"], "kv_dtype": w["kv_dtype"],
                    "context_len_mean": sum(lens) / len(lens), "context_len_max": max_len,
                    "kv_bytes_per_step": step_bytes,
-                   "step": "store_kv(new tokens) + decode (split + merge)",
+                   "step": "store_kv(new tokens) + decode",
                    "l2": f"rotating {n_pools} KV pools, {n_pools * step_bytes / 1e9:.2f} GB of KV "
                          f"between reuses > 129 MB L2",
                    "parallelism": f"replicas x{world} (sequences sharded, no collective)"},
@@ -430,7 +431,8 @@ def run_gpu(args, world, rank, local):
         "hbm_frac_of_peak": value / peak,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
-                     "kernel": "pa_decode (split + merge launches, CUDA events per call)",
+                     "kernel": "pa_decode (decode_persistent_kernel, CUDA events per call)",
+                     "traffic_source": "profiles/decode_persistent_kernel_" + name + ".md",
                      "peak_kind": f"of {peak_kind}"},
         "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
