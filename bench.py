@@ -1,14 +1,16 @@
 """Benchmark of the paged decode hot path on GB300.
 
-One step = pa_store_kv of the batch's new tokens + pa_decode over the whole
-batch (split kernel and, when a sequence needs several splits, the merge
-kernel), on the Llama-3-8B-shaped workload (batch 64, 32/8 heads, head_dim 128,
-block_size 16, context_len ~ U[512, 4096]) unless --workload says otherwise.
+One step = the append of the batch's new tokens to the cache + decode
+attention over the whole batch, by default through pa_decode_append (one
+persistent launch that stores each new row while attending; --step separate
+times pa_store_kv + pa_decode instead), on the Llama-3-8B-shaped workload
+(batch 64, 32/8 heads, head_dim 128, block_size 16, context_len ~ U[512, 4096])
+unless --workload says otherwise.
 
 Prints ONE JSON line (rank 0). Inputs are resident in HBM before timing; the
 step rotates over several independently drawn KV pools so consecutive steps
-never re-read KV from L2. The dominant launch (pa_decode) is also timed on its
-own with CUDA events inside the timed region for the roofline figure.
+never re-read KV from L2. The decode launch is also timed on its own with CUDA
+events inside the timed region for the roofline figure.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
   python bench.py --impl reference ...   # the CPU oracle as the reference arm
@@ -317,7 +319,19 @@ def run_gpu(args, world, rank, local):
     out = torch.empty((B, w["num_heads"], w["head_dim"]), dtype=torch.bfloat16, device=dev)
     stream = torch.cuda.current_stream()
 
+    fused = args.step == "append"
+
     def step(p, ev=None):
+        if fused:
+            if ev is not None:
+                ev[0].record(stream)
+            pa.decode_append(p.q, p.k_new, p.v_new, p.k_cache, p.v_cache, p.block_tables,
+                             p.context_lens, p.scale, max_context_len=max_len, out=out,
+                             workspace=workspace, k_scale_new=p.k_scale_new,
+                             v_scale_new=p.v_scale_new, k_scale=p.k_scale, v_scale=p.v_scale)
+            if ev is not None:
+                ev[1].record(stream)
+            return
         pa.store_kv(p.k_new, p.v_new, p.slot_mapping, p.k_cache, p.v_cache, p.k_scale_new,
                     p.v_scale_new, p.k_scale, p.v_scale)
         if ev is not None:
@@ -362,8 +376,10 @@ def run_gpu(args, world, rank, local):
 
     # ---------------- end to end through the public API with host buffers
     p0 = pools[0]
-    host = {k: getattr(p0, k).cpu().pin_memory()
-            for k in ("q", "k_new", "v_new", "slot_mapping", "block_tables", "context_lens")}
+    host_keys = ("q", "k_new", "v_new", "block_tables", "context_lens")
+    if not fused:
+        host_keys += ("slot_mapping",)
+    host = {k: getattr(p0, k).cpu().pin_memory() for k in host_keys}
     if fp8:
         host["k_scale_new"] = p0.k_scale_new.cpu().pin_memory()
         host["v_scale_new"] = p0.v_scale_new.cpu().pin_memory()
@@ -375,6 +391,15 @@ def run_gpu(args, world, rank, local):
     def e2e_step(p):
         for k, v in host.items():
             dev_in[k].copy_(v, non_blocking=True)
+        if fused:
+            pa.decode_append(dev_in["q"], dev_in["k_new"], dev_in["v_new"], p.k_cache,
+                             p.v_cache, dev_in["block_tables"], dev_in["context_lens"], p.scale,
+                             max_context_len=max_len, out=out, workspace=workspace,
+                             k_scale_new=dev_in.get("k_scale_new"),
+                             v_scale_new=dev_in.get("v_scale_new"), k_scale=p.k_scale,
+                             v_scale=p.v_scale)
+            out_host.copy_(out, non_blocking=True)
+            return
         pa.store_kv(dev_in["k_new"], dev_in["v_new"], dev_in["slot_mapping"], p.k_cache,
                     p.v_cache, dev_in.get("k_scale_new"), dev_in.get("v_scale_new"), p.k_scale,
                     p.v_scale)
@@ -409,8 +434,9 @@ def run_gpu(args, world, rank, local):
     peak, peak_kind = peaks()
     achieved = step_bytes / (dec_avg_ms / 1e3) / 1e9
     traffic = traffic_from_profile("pa_decode.cu", name)
-    # store_kv + decode; the grid-split path (batches above 2048) adds a merge
-    n_launch = 2 if B <= 2048 else 3
+    # store_kv + decode (or the fused append: one persistent launch); the
+    # grid-split path (batches above 2048) adds a merge
+    n_launch = (1 if fused else 2) if B <= 2048 else 3
     clocks = sampler.summary(t_wall0, t_wall1) if sampler else None
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
@@ -422,7 +448,8 @@ def run_gpu(args, world, rank, local):
                    "block_size": w["block_size"], "kv_dtype": w["kv_dtype"],
                    "context_len_mean": sum(lens) / len(lens), "context_len_max": max_len,
                    "kv_bytes_per_step": step_bytes,
-                   "step": "store_kv(new tokens) + decode",
+                   "step": ("decode_append (store of the new tokens fused into decode)"
+                            if fused else "store_kv(new tokens) + decode"),
                    "l2": f"rotating {n_pools} KV pools, {n_pools * step_bytes / 1e9:.2f} GB of KV "
                          f"between reuses > 129 MB L2",
                    "parallelism": f"replicas x{world} (sequences sharded, no collective)"},
@@ -431,7 +458,8 @@ def run_gpu(args, world, rank, local):
         "hbm_frac_of_peak": value / peak,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
-                     "kernel": "pa_decode (decode_persistent_kernel, CUDA events per call)",
+                     "kernel": ("pa_decode_append" if fused else "pa_decode") +
+                               " (decode_persistent_kernel, CUDA events per call)",
                      "traffic_source": "profiles/decode_persistent_kernel_" + name + ".md",
                      "peak_kind": f"of {peak_kind}"},
         "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d,
@@ -539,6 +567,8 @@ def main():
     ap.add_argument("--impl", choices=["gpu", "reference"], default="gpu")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(W.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--step", choices=["append", "separate"], default="append",
+                    help="decode step: fused pa_decode_append, or pa_store_kv + pa_decode")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

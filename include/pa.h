@@ -1,7 +1,7 @@
 /*
  * pa.h - C ABI of the GB300 (sm_103a) paged-KV-cache attention library.
  *
- * Three operations, as the source pages define them:
+ * The operations, as the source pages define them:
  *   pa_store_kv        append new tokens' K/V to their cache slots
  *                      ("tiny-vllm part 05", section "Gathering K/V into a
  *                      batched buffer and scattering into blocks"; the
@@ -13,6 +13,8 @@
  *                      Pass", sections 2-4 and the zero-padding caveat;
  *                      "Decode Phase" glossary, the q.K^T / softmax / sum-of-V
  *                      steps).
+ *   pa_decode_append   pa_store_kv of each sequence's new token followed by
+ *                      pa_decode, fused into one persistent kernel.
  *   pa_prefill_varlen  packed varlen prefill over a prefix already in the
  *                      paged cache, bottom-right-aligned causal mask
  *                      ("Prefill Forward Prefix Caching Explained", Facts 1-2
@@ -143,6 +145,35 @@ pa_status pa_decode(const void* q, const pa_kv_cache* cache, const int32_t* bloc
                     int32_t max_blocks_per_seq, const int32_t* context_lens,
                     int32_t max_context_len, int32_t batch, int32_t num_heads, float scale,
                     void* out, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * pa_decode_append - one decode step's store and attention in one call: the
+ * store_kvcache step (each sequence's new K/V row written to the cache) then
+ * attention over context_len keys, new token included ("Decode Phase
+ * Attention Forward Pass", section 2, the store-then-attend order).
+ *   k_new, v_new    (batch, num_kv_heads, head_dim), cache dtype, device,
+ *                   16-byte aligned: the new token of sequence b.
+ *   k_scale_new,    (batch, num_kv_heads) fp32, FP8 caches only (else NULL).
+ *   v_scale_new
+ *   other arguments as pa_decode (same workspace size).
+ * The row goes to position p = min(context_len, bound) - 1 of its sequence,
+ * i.e. slot block_tables[b][p / block_size] * block_size + p % block_size,
+ * where bound is max_context_len (or the block-table capacity); a sequence
+ * with context_len 0 appends nothing. Result and cache contents are those of
+ * pa_store_kv with that slot mapping followed by pa_decode. The block holding
+ * position p must not be read by another sequence of the same call. A
+ * physical block id out of range skips the write and sets
+ * PA_DEVERR_BLOCK_RANGE. With the persistent kernel (batch <= 2048) the warp
+ * that attends to a sequence's last block also writes the row; larger batches
+ * use a separate store launch first.
+ */
+pa_status pa_decode_append(const void* q, const void* k_new, const void* v_new,
+                           const float* k_scale_new, const float* v_scale_new,
+                           const pa_kv_cache* cache, const int32_t* block_tables,
+                           int32_t max_blocks_per_seq, const int32_t* context_lens,
+                           int32_t max_context_len, int32_t batch, int32_t num_heads,
+                           float scale, void* out, void* workspace, size_t workspace_bytes,
+                           void* stream);
 
 /*
  * pa_prefill_varlen - prefill attention of packed new tokens over their

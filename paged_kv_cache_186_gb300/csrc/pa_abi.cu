@@ -225,10 +225,17 @@ size_t pa_decode_workspace_size(const pa_kv_cache* cache, int32_t batch, int32_t
       .workspace_bytes;
 }
 
-pa_status pa_decode(const void* q, const pa_kv_cache* cache, const int32_t* block_tables,
-                    int32_t max_blocks_per_seq, const int32_t* context_lens,
-                    int32_t max_context_len, int32_t batch, int32_t num_heads, float scale,
-                    void* out, void* workspace, size_t workspace_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// Shared body of pa_decode and pa_decode_append (k_new == NULL: no append).
+pa_status decode_common(const void* q, const pa_kv_cache* cache, const int32_t* block_tables,
+                        int32_t max_blocks_per_seq, const int32_t* context_lens,
+                        int32_t max_context_len, int32_t batch, int32_t num_heads, float scale,
+                        void* out, void* workspace, size_t workspace_bytes, void* stream,
+                        const void* k_new, const void* v_new, const float* k_scale_new,
+                        const float* v_scale_new) {
   pa_status st = check_cache(cache);
   if (st != PA_OK) return st;
   if (batch < 0 || num_heads <= 0 || max_blocks_per_seq <= 0) return PA_ERR_SHAPE;
@@ -254,8 +261,39 @@ pa_status pa_decode(const void* q, const pa_kv_cache* cache, const int32_t* bloc
   CUtensorMap kmap, vmap;
   if ((st = cached_cache_map(&kmap, cache->k_cache, cache)) != PA_OK) return st;
   if ((st = cached_cache_map(&vmap, cache->v_cache, cache)) != PA_OK) return st;
+  const cudaStream_t strm = static_cast<cudaStream_t>(stream);
+  const bool fused_append = k_new != nullptr && plan.persistent_ctas > 0;
+  if (k_new != nullptr && !fused_append) {
+    // grid-split path: append with its own launch first, then attend
+    pa::StoreArgs s{};
+    s.k = k_new;
+    s.v = v_new;
+    s.k_scale_new = k_scale_new;
+    s.v_scale_new = v_scale_new;
+    s.k_cache = cache->k_cache;
+    s.v_cache = cache->v_cache;
+    s.k_scale = fp8 ? cache->k_scale : nullptr;
+    s.v_scale = fp8 ? cache->v_scale : nullptr;
+    s.num_tokens = batch;
+    s.row_bytes = cache->num_kv_heads * cache->head_dim * elem_bytes(cache);
+    s.num_kv_heads = cache->num_kv_heads;
+    s.block_size = cache->block_size;
+    s.num_slots = static_cast<long long>(cache->num_blocks) * cache->block_size;
+    s.err = dev->err;
+    if (pa::launch_store_new_tokens(s, block_tables, max_blocks_per_seq, context_lens, cap,
+                                    strm) != cudaSuccess)
+      return PA_ERR_CUDA;
+  }
   pa::DecodeArgs a{};
   a.q = q;
+  if (fused_append) {
+    a.k_new = k_new;
+    a.v_new = v_new;
+    a.k_scale_new = fp8 ? k_scale_new : nullptr;
+    a.v_scale_new = fp8 ? v_scale_new : nullptr;
+    a.k_cache = cache->k_cache;
+    a.v_cache = cache->v_cache;
+  }
   a.block_tables = block_tables;
   a.context_lens = context_lens;
   a.k_scale = fp8 ? cache->k_scale : nullptr;
@@ -289,9 +327,38 @@ pa_status pa_decode(const void* q, const pa_kv_cache* cache, const int32_t* bloc
   a.num_splits = plan.num_splits;
   a.fp8 = fp8;
   a.scale_log2 = scale * 1.4426950408889634f;  // log2(e): scores kept in base-2 units
-  return pa::launch_decode(a, kmap, vmap, static_cast<cudaStream_t>(stream)) == cudaSuccess
-             ? PA_OK
-             : PA_ERR_CUDA;
+  return pa::launch_decode(a, kmap, vmap, strm) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+pa_status pa_decode(const void* q, const pa_kv_cache* cache, const int32_t* block_tables,
+                    int32_t max_blocks_per_seq, const int32_t* context_lens,
+                    int32_t max_context_len, int32_t batch, int32_t num_heads, float scale,
+                    void* out, void* workspace, size_t workspace_bytes, void* stream) {
+  return decode_common(q, cache, block_tables, max_blocks_per_seq, context_lens, max_context_len,
+                       batch, num_heads, scale, out, workspace, workspace_bytes, stream, nullptr,
+                       nullptr, nullptr, nullptr);
+}
+
+pa_status pa_decode_append(const void* q, const void* k_new, const void* v_new,
+                           const float* k_scale_new, const float* v_scale_new,
+                           const pa_kv_cache* cache, const int32_t* block_tables,
+                           int32_t max_blocks_per_seq, const int32_t* context_lens,
+                           int32_t max_context_len, int32_t batch, int32_t num_heads,
+                           float scale, void* out, void* workspace, size_t workspace_bytes,
+                           void* stream) {
+  pa_status st = check_cache(cache);
+  if (st != PA_OK) return st;
+  if (batch > 0 && (k_new == nullptr || v_new == nullptr)) return PA_ERR_NULL;
+  const bool fp8 = cache->dtype == PA_KV_FP8_E4M3;
+  if (fp8 != (k_scale_new != nullptr) || fp8 != (v_scale_new != nullptr)) return PA_ERR_DTYPE;
+  if (batch > 0 && (!aligned16(k_new) || !aligned16(v_new))) return PA_ERR_ALIGN;
+  return decode_common(q, cache, block_tables, max_blocks_per_seq, context_lens, max_context_len,
+                       batch, num_heads, scale, out, workspace, workspace_bytes, stream, k_new,
+                       v_new, k_scale_new, v_scale_new);
 }
 
 pa_status pa_prefill_varlen(const void* q, const pa_kv_cache* cache, const int32_t* block_tables,

@@ -590,6 +590,49 @@ struct PCfg {
   static int smem_bytes(int batch) { return 1024 + kPrefixOff + (batch + 1) * 4; }
 };
 
+// Fused append (pa_decode_append): the new token of segment (b, kvh) is row t
+// of its last block. The warp that attends to that block copies the row from
+// k_new / v_new (row `bk` = b * Hkv + kvh) into the staged tile (and the FP8
+// scales into the staged scales) and into the cache slot. Kept out of line:
+// it runs once per segment and must not add registers to the block loop.
+template <int D, int BS, bool FP8>
+__device__ __noinline__ void append_row(uint8_t* tile, float* stage_scales, const int32_t* bt_entry,
+                                        int bk, int t, const DecodeArgs a, int lane) {
+  constexpr int kRowBytes = D * (FP8 ? 1 : 2);
+  constexpr int kChunks = kRowBytes / 16;
+  constexpr int kTile = (kRowBytes / kSwizzleBytes) * BS * kSwizzleBytes;
+  const int phys = *bt_entry;
+  const bool phys_ok = phys >= 0 && phys < a.num_blocks;
+  const int Hkv = a.num_kv_heads, kvh = bk % Hkv;
+  if (lane < 2 * kChunks) {
+    const bool isv = lane >= kChunks;
+    const int c = isv ? lane - kChunks : lane;
+    const uint4 val = *reinterpret_cast<const uint4*>(
+        static_cast<const uint8_t*>(isv ? a.v_new : a.k_new) +
+        static_cast<long long>(bk) * kRowBytes + 16 * c);
+    *reinterpret_cast<uint4*>(tile + (isv ? kTile : 0) + (swz<BS>(0, t, c))) = val;
+    if (phys_ok)
+      *reinterpret_cast<uint4*>(static_cast<uint8_t*>(isv ? a.v_cache : a.k_cache) +
+                                ((static_cast<long long>(phys) * BS + t) * Hkv + kvh) * kRowBytes +
+                                16 * c) = val;
+  }
+  if constexpr (FP8) {
+    if (lane == 0) {
+      const float kn = a.k_scale_new[bk], vn = a.v_scale_new[bk];
+      stage_scales[t] = kn;
+      stage_scales[BS + t] = vn;
+      if (phys_ok) {
+        const long long so = (static_cast<long long>(phys) * Hkv + kvh) * BS + t;
+        const_cast<float*>(a.k_scale)[so] = kn;
+        const_cast<float*>(a.v_scale)[so] = vn;
+      }
+    }
+  }
+  if (lane == 0 && !phys_ok) report_error(a.err, PA_DEVERR_BLOCK_RANGE);
+  fence_proxy_async_smem();  // generic writes before the stage's next TMA refill
+  __syncwarp();
+}
+
 template <int D, int BS, int NW, int ST, bool FP8>
 __global__ void __launch_bounds__(NW * 32, 3)
     decode_persistent_kernel(const __grid_constant__ CUtensorMap kmap,
@@ -744,6 +787,11 @@ __global__ void __launch_bounds__(NW * 32, 3)
       }
       const uint32_t kt = stage0 + s * C::kStage;
       const float* ksc = scale_ptr + ((warp * ST + s) * 2) * BS;
+      if (a.k_new != nullptr && blk == cp.nblk - 1)
+        append_row<D, BS, FP8>(base_ptr + (kt - base),
+                               const_cast<float*>(scale_ptr) + ((warp * ST + s) * 2) * BS,
+                               a.block_tables + static_cast<long long>(cp.b) * a.max_blocks + blk,
+                               cp.b * Hkv + cp.kvh, (L - 1) - blk * BS, a, lane);
       attend_block<D, BS, FP8>(kt, kt + C::kTile, base_ptr, base, ksc, ksc + BS, blk * BS, L, qa,
                                acc, m_run, l_run, sl2, lane);
       ++consumed;

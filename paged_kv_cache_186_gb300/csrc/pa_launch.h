@@ -28,6 +28,13 @@ struct StoreArgs {
 
 cudaError_t launch_store_kv(const StoreArgs& a, cudaStream_t stream);
 
+// Append each sequence's new token at position context_lens[b]-1 (slot from
+// the block table): used by the fused append when the persistent decode does
+// not apply. `a.slot_mapping` is ignored; the cache fields of `a` are used.
+cudaError_t launch_store_new_tokens(const StoreArgs& a, const int32_t* block_tables,
+                                    int max_blocks, const int32_t* context_lens, int len_cap,
+                                    cudaStream_t stream);
+
 // Largest batch the persistent decode kernel handles (its per-sequence block
 // prefix sums live in shared memory); larger batches use the grid-split kernel.
 constexpr int kMaxPersistentBatch = 2048;
@@ -45,6 +52,14 @@ struct DecodeArgs {
   unsigned long long* seg_counters;  // persistent path: (B*Hkv) arrival counters
   uint32_t epoch;             // persistent path: tag of this call in seg_counters
   uint32_t* err;
+  // fused append (pa_decode_append): the new token of sequence b, at position
+  // context_lens[b]-1, is written to the cache by the warp that attends to it
+  const void* k_new;          // (B, Hkv, D) cache dtype, or NULL
+  const void* v_new;
+  const float* k_scale_new;   // FP8: (B, Hkv)
+  const float* v_scale_new;
+  void* k_cache;              // cache base pointers (written when appending)
+  void* v_cache;
   int batch, num_heads, num_kv_heads, group, head_dim, block_size;
   int max_blocks, num_blocks, len_cap;
   int persistent_ctas;        // > 0: persistent kernel with this many CTAs

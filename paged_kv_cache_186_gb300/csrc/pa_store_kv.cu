@@ -51,7 +51,59 @@ __global__ void __launch_bounds__(kStoreWarps * 32) store_kv_kernel(const StoreA
   }
 }
 
+// One warp per sequence: slot of position context_len-1 from the block table,
+// then the same row copies as store_kv_kernel.
+__global__ void __launch_bounds__(kStoreWarps * 32)
+    store_new_tokens_kernel(const StoreArgs a, const int32_t* block_tables, int max_blocks,
+                            const int32_t* context_lens, int len_cap) {
+  grid_launch_dependents();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * kStoreWarps + warp;
+  if (t >= a.num_tokens) return;
+  const int L = min(context_lens[t], len_cap);
+  if (L <= 0) return;
+  const int logical = (L - 1) / a.block_size;
+  if (logical >= max_blocks) return;
+  const long long phys = block_tables[static_cast<long long>(t) * max_blocks + logical];
+  const long long slot = phys * a.block_size + (L - 1) % a.block_size;
+  if (phys < 0 || slot >= a.num_slots) {
+    if (lane == 0) report_error(a.err, PA_DEVERR_BLOCK_RANGE);
+    return;
+  }
+  const int n16 = a.row_bytes >> 4;
+  const uint4* ks = reinterpret_cast<const uint4*>(static_cast<const char*>(a.k) +
+                                                   static_cast<long long>(t) * a.row_bytes);
+  const uint4* vs = reinterpret_cast<const uint4*>(static_cast<const char*>(a.v) +
+                                                   static_cast<long long>(t) * a.row_bytes);
+  uint4* kd = reinterpret_cast<uint4*>(static_cast<char*>(a.k_cache) + slot * a.row_bytes);
+  uint4* vd = reinterpret_cast<uint4*>(static_cast<char*>(a.v_cache) + slot * a.row_bytes);
+  for (int i = lane; i < n16; i += 32) {
+    const uint4 kv = __ldg(ks + i);
+    const uint4 vv = __ldg(vs + i);
+    kd[i] = kv;
+    vd[i] = vv;
+  }
+  if (a.k_scale != nullptr) {
+    const long long off = slot % a.block_size;
+    for (int h = lane; h < a.num_kv_heads; h += 32) {
+      const long long dst = (phys * a.num_kv_heads + h) * a.block_size + off;
+      a.k_scale[dst] = a.k_scale_new[static_cast<long long>(t) * a.num_kv_heads + h];
+      a.v_scale[dst] = a.v_scale_new[static_cast<long long>(t) * a.num_kv_heads + h];
+    }
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_store_new_tokens(const StoreArgs& a, const int32_t* block_tables,
+                                    int max_blocks, const int32_t* context_lens, int len_cap,
+                                    cudaStream_t stream) {
+  if (a.num_tokens <= 0) return cudaSuccess;
+  const int grid = (a.num_tokens + kStoreWarps - 1) / kStoreWarps;
+  store_new_tokens_kernel<<<grid, kStoreWarps * 32, 0, stream>>>(a, block_tables, max_blocks,
+                                                                 context_lens, len_cap);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_store_kv(const StoreArgs& a, cudaStream_t stream) {
   if (a.num_tokens <= 0) return cudaSuccess;
