@@ -479,17 +479,20 @@ __device__ __forceinline__ SegParts seg_parts(const int* prefix, int B, int Hkv,
 // Count this warp's arrival at segment `seg` (64-bit counter: call epoch in
 // the high word, arrivals of that call in the low word; a counter left by an
 // earlier call restarts at 1). Returns true for the last of `parts` arrivals.
+// A counter that already carries this call's epoch takes a plain atomic add
+// (arrivals of many warps at once are then not serialised by compare-and-swap
+// retries); only a stale counter is re-tagged with a compare-and-swap.
 __device__ __forceinline__ bool arrive_last(unsigned long long* counter, uint32_t epoch,
                                             uint32_t parts, uint32_t* err) {
   unsigned long long old = atomicAdd(counter, 0ull);
 #pragma unroll 1
-  for (int it = 0; it < (1 << 20); ++it) {
-    const unsigned long long nv = (static_cast<uint32_t>(old >> 32) == epoch)
-                                      ? old + 1
-                                      : ((static_cast<unsigned long long>(epoch) << 32) | 1ull);
-    const unsigned long long prev = atomicCAS(counter, old, nv);
-    if (prev == old) return static_cast<uint32_t>(nv) == parts;
-    old = prev;
+  for (int it = 0; it < 64; ++it) {
+    if (static_cast<uint32_t>(old >> 32) == epoch)
+      return static_cast<uint32_t>(atomicAdd(counter, 1ull) + 1ull) == parts;
+    const unsigned long long tagged = (static_cast<unsigned long long>(epoch) << 32) | 1ull;
+    const unsigned long long prev = atomicCAS(counter, old, tagged);
+    if (prev == old) return parts == 1u;
+    old = prev;  // re-tagged by another arrival of this call (or changed): retry
   }
   report_error(err, PA_DEVERR_WAIT_TIMEOUT);
   return false;
@@ -702,6 +705,9 @@ __global__ void __launch_bounds__(NW * 32, 3)
 
   const uint32_t bar0 = smem_addr(&bars[warp * ST]);
   const uint32_t stage0 = base + warp * ST * C::kStage;
+  // K/V are read once per call: keep them from evicting the block tables,
+  // lengths, q and split partials that later reads want from L2
+  const uint64_t l2_policy = l2_evict_first_policy();
   if (lane == 0) {
     for (int s = 0; s < ST; ++s) mbar_init(bar0 + 8 * s, 1);
     fence_barrier_init();
@@ -709,31 +715,44 @@ __global__ void __launch_bounds__(NW * 32, 3)
   }
   __syncwarp();
 
-  // ---- producer: this warp's blocks in order across pieces; the block id of
-  // the next load is fetched one step before it is needed
-  Piece pp;
-  piece_first(pp, prefix, B, Hkv, r0, r1);
-  int pp_next = pp.lo;
-  bool pend = false;
-  int pend_kvh = 0, pend_phys = 0;
-  auto fetch_next = [&]() {
-    pend = false;
-    while (pp.valid) {
-      if (pp_next < pp.hi) {
-        pend = true;
-        pend_kvh = pp.kvh;
-        pend_phys = a.block_tables[static_cast<long long>(pp.b) * a.max_blocks + pp_next];
-        ++pp_next;
-        return;
+  // ---- producer: this warp's blocks in order. Block ids come 32 at a time:
+  // lane i holds the kv head and physical block of the warp's block
+  // win_base + i; the next window's table reads are in flight while the
+  // current window is used, so no TMA issue waits for a block-table read.
+  const long long nmine = r1 - r0;
+  auto load_window = [&](long long wbase, int& kvh_o, int& phys_o) {
+    kvh_o = 0;
+    phys_o = 0;
+    const long long r = r0 + wbase + lane;
+    if (r < r1) {
+      int lo = 0, hi = B - 1;  // last b with prefix[b] * Hkv <= r (it has blocks)
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (static_cast<long long>(prefix[mid]) * Hkv <= r) lo = mid;
+        else hi = mid - 1;
       }
-      piece_next(pp, prefix, B, Hkv, r1);
-      pp_next = pp.lo;
+      const int nb = prefix[lo + 1] - prefix[lo];
+      const long long off = r - static_cast<long long>(prefix[lo]) * Hkv;
+      kvh_o = static_cast<int>(off / nb);
+      phys_o = a.block_tables[static_cast<long long>(lo) * a.max_blocks + off % nb];
     }
   };
+  int cur_kvh, cur_phys, nxt_kvh, nxt_phys;
+  load_window(0, cur_kvh, cur_phys);
+  load_window(32, nxt_kvh, nxt_phys);
+  long long win_base = 0;
   int issued = 0;
   auto issue_pending = [&]() {
-    if (!pend) return;
-    int phys = pend_phys;
+    if (issued >= nmine) return;
+    if (issued - win_base == 32) {
+      win_base += 32;
+      cur_kvh = nxt_kvh;
+      cur_phys = nxt_phys;
+      load_window(win_base + 32, nxt_kvh, nxt_phys);
+    }
+    const int i = static_cast<int>(issued - win_base);
+    const int kvh = __shfl_sync(kFull, cur_kvh, i);
+    int phys = __shfl_sync(kFull, cur_phys, i);
     if (phys < 0 || phys >= a.num_blocks) {
       if (lane == 0) report_error(a.err, PA_DEVERR_BLOCK_RANGE);
       phys = 0;  // stay inside the pool; the result is flagged as invalid
@@ -745,22 +764,20 @@ __global__ void __launch_bounds__(NW * 32, 3)
       mbar_arrive_expect_tx(bar, C::kTx);
 #pragma unroll
       for (int j = 0; j < C::kNSub; ++j) {
-        tma_load_3d(kt + j * C::kSubBytes, &kmap, bar, j * (kSwizzleBytes / C::kElem), pend_kvh,
-                    phys * BS);
+        tma_load_3d(kt + j * C::kSubBytes, &kmap, bar, j * (kSwizzleBytes / C::kElem), kvh,
+                    phys * BS, l2_policy);
         tma_load_3d(kt + C::kTile + j * C::kSubBytes, &vmap, bar,
-                    j * (kSwizzleBytes / C::kElem), pend_kvh, phys * BS);
+                    j * (kSwizzleBytes / C::kElem), kvh, phys * BS, l2_policy);
       }
       if constexpr (FP8) {
-        const long long off = (static_cast<long long>(phys) * Hkv + pend_kvh) * BS;
+        const long long off = (static_cast<long long>(phys) * Hkv + kvh) * BS;
         const uint32_t sc = scale_base + ((warp * ST + s) * 2) * BS * 4;
-        bulk_load(sc, a.k_scale + off, BS * 4, bar);
-        bulk_load(sc + BS * 4, a.v_scale + off, BS * 4, bar);
+        bulk_load(sc, a.k_scale + off, BS * 4, bar, l2_policy);
+        bulk_load(sc + BS * 4, a.v_scale + off, BS * 4, bar, l2_policy);
       }
     }
     ++issued;
-    fetch_next();
   };
-  fetch_next();
   for (int s = 0; s < ST; ++s) issue_pending();
 
   // ---- consumer: pieces in order
