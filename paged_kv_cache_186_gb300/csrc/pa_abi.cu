@@ -299,14 +299,12 @@ pa_status decode_common(const void* q, const pa_kv_cache* cache, const int32_t* 
   a.k_scale = fp8 ? cache->k_scale : nullptr;
   a.v_scale = fp8 ? cache->v_scale : nullptr;
   a.out = out;
+  a.slot_rows = plan.slot_rows;
   if (plan.workspace_bytes > 0) {
-    const size_t slots = plan.persistent_ctas > 0
-                             ? 2 * static_cast<size_t>(plan.persistent_slots_per_cta) *
-                                   plan.persistent_ctas
-                             : static_cast<size_t>(batch) * cache->num_kv_heads * plan.num_splits;
+    const size_t rows = plan.partial_slots * plan.slot_rows;
     a.part_o = static_cast<float*>(workspace);
-    a.part_ml = a.part_o + slots * 8 * cache->head_dim;
-    a.prefix_out = reinterpret_cast<int*>(a.part_ml + slots * 8 * 2);
+    a.part_ml = a.part_o + rows * cache->head_dim;
+    a.prefix_out = reinterpret_cast<int*>(a.part_ml + rows * 2);
     // 8-byte aligned arrival counters after the prefix sums
     const uintptr_t cp = reinterpret_cast<uintptr_t>(a.prefix_out + batch + 1);
     a.seg_counters = reinterpret_cast<unsigned long long*>((cp + 15) & ~static_cast<uintptr_t>(15));

@@ -428,7 +428,7 @@ __device__ __forceinline__ void write_warp_result(const DecodeArgs& a, int b, in
     }
     return;
   }
-  float* po = a.part_o + slot * 8 * D;
+  float* po = a.part_o + slot * a.slot_rows * D;
 #pragma unroll
   for (int mt = 0; mt < D / 16; ++mt) {
     int d0, d1;
@@ -444,8 +444,8 @@ __device__ __forceinline__ void write_warp_result(const DecodeArgs& a, int b, in
     }
   }
   if (q4 == 0 && r < G) {
-    a.part_ml[(slot * 8 + r) * 2 + 0] = m_run;
-    a.part_ml[(slot * 8 + r) * 2 + 1] = l_tot;
+    a.part_ml[(slot * a.slot_rows + r) * 2 + 0] = m_run;
+    a.part_ml[(slot * a.slot_rows + r) * 2 + 1] = l_tot;
   }
 }
 
@@ -476,26 +476,50 @@ __device__ __forceinline__ SegParts seg_parts(const int* prefix, int B, int Hkv,
   return sp;
 }
 
-// Count this warp's arrival at segment `seg` (64-bit counter: call epoch in
-// the high word, arrivals of that call in the low word; a counter left by an
-// earlier call restarts at 1). Returns true for the last of `parts` arrivals.
-// A counter that already carries this call's epoch takes a plain atomic add
-// (arrivals of many warps at once are then not serialised by compare-and-swap
-// retries); only a stale counter is re-tagged with a compare-and-swap.
-__device__ __forceinline__ bool arrive_last(unsigned long long* counter, uint32_t epoch,
-                                            uint32_t parts, uint32_t* err) {
-  unsigned long long old = atomicAdd(counter, 0ull);
+// Epoch-tagged counters in the caller's workspace (contents on entry are
+// arbitrary): the high word holds the call's epoch, the low word the count of
+// this call. Every counter is tagged early in the call (tag_counters), so an
+// arrival is normally one atomic add. An add that still finds another call's
+// epoch tags the word itself with a compare-and-swap (whoever tags first wins;
+// nothing resets a tagged word) and counts itself again.
+__device__ __forceinline__ uint32_t tagged_fetch_add(unsigned long long* counter, uint32_t epoch,
+                                                     uint32_t* err) {
+  const unsigned long long old = atomicAdd(counter, 1ull);
+  if (static_cast<uint32_t>(old >> 32) == epoch) return static_cast<uint32_t>(old);
+  unsigned long long cur = old + 1ull;
 #pragma unroll 1
-  for (int it = 0; it < 64; ++it) {
-    if (static_cast<uint32_t>(old >> 32) == epoch)
-      return static_cast<uint32_t>(atomicAdd(counter, 1ull) + 1ull) == parts;
-    const unsigned long long tagged = (static_cast<unsigned long long>(epoch) << 32) | 1ull;
-    const unsigned long long prev = atomicCAS(counter, old, tagged);
-    if (prev == old) return parts == 1u;
-    old = prev;  // re-tagged by another arrival of this call (or changed): retry
+  for (int it = 0; it < (1 << 14); ++it) {
+    if (static_cast<uint32_t>(cur >> 32) == epoch)
+      return static_cast<uint32_t>(atomicAdd(counter, 1ull));
+    const unsigned long long prev =
+        atomicCAS(counter, cur, (static_cast<unsigned long long>(epoch) << 32) | 1ull);
+    if (prev == cur) return 0u;
+    cur = prev;
   }
   report_error(err, PA_DEVERR_WAIT_TIMEOUT);
-  return false;
+  return 0xffffffffu;
+}
+
+// Tag counters [lo, hi) with this call's epoch and a zero count, unless
+// already tagged (one lane per counter).
+__device__ __forceinline__ void tag_counters(unsigned long long* counters, long long lo,
+                                             long long hi, uint32_t epoch, int lane) {
+  const unsigned long long tagged = static_cast<unsigned long long>(epoch) << 32;
+  for (long long i = lo + lane; i < hi; i += 32) {
+    unsigned long long cur = atomicAdd(counters + i, 0ull);
+#pragma unroll 1
+    for (int it = 0; it < 8 && static_cast<uint32_t>(cur >> 32) != epoch; ++it) {
+      const unsigned long long prev = atomicCAS(counters + i, cur, tagged);
+      if (prev == cur) break;
+      cur = prev;
+    }
+  }
+}
+
+// Count this warp's arrival at a segment of `parts` pieces; true for the last.
+__device__ __forceinline__ bool arrive_last(unsigned long long* counter, uint32_t epoch,
+                                            uint32_t parts, uint32_t* err) {
+  return tagged_fetch_add(counter, epoch, err) + 1u == parts;
 }
 
 // Merge the partials of segment (b, kvh) and write its bf16 rows:
@@ -518,7 +542,8 @@ __device__ __forceinline__ void merge_segment_g(const DecodeArgs& a, const SegPa
   for (int j0 = 0; j0 < sp.n; j0 += PR) {
     const int j = j0 + j_l;
     if (j < sp.n && g_ok) {
-      const float2 ml = __ldcg(reinterpret_cast<const float2*>(a.part_ml + (sp.slot(j) * 8 + g_l) * 2));
+      const float2 ml =
+          __ldcg(reinterpret_cast<const float2*>(a.part_ml + (sp.slot(j) * GP + g_l) * 2));
       const float m2 = fmaxf(M, ml.x);
       L = L * fast_exp2(M - m2) + ml.y * fast_exp2(ml.x - m2);
       M = m2;
@@ -542,14 +567,14 @@ __device__ __forceinline__ void merge_segment_g(const DecodeArgs& a, const SegPa
   for (int j0 = 0; j0 < sp.n; j0 += PR) {
     float f = 0.f;
     const int j = j0 + j_l;
-    if (j < sp.n && g_ok) f = fast_exp2(__ldcg(a.part_ml + (sp.slot(j) * 8 + g_l) * 2) - M);
+    if (j < sp.n && g_ok) f = fast_exp2(__ldcg(a.part_ml + (sp.slot(j) * GP + g_l) * 2) - M);
 #pragma unroll
     for (int jj = 0; jj < PR; ++jj) {
 #pragma unroll
       for (int g = 0; g < GP; ++g) {
         const float fv = __shfl_sync(kFull, f, jj * GP + g);
         if (j0 + jj < sp.n && g < G) {
-          const float* src = a.part_o + (sp.slot(j0 + jj) * 8 + g) * D + lane * V;
+          const float* src = a.part_o + (sp.slot(j0 + jj) * GP + g) * D + lane * V;
           if constexpr (V == 4) {
             const float4 x = __ldcg(reinterpret_cast<const float4*>(src));
             acc[g][0] += fv * x.x; acc[g][1] += fv * x.y; acc[g][2] += fv * x.z; acc[g][3] += fv * x.w;
@@ -779,6 +804,13 @@ __global__ void __launch_bounds__(NW * 32, 3)
     ++issued;
   };
   for (int s = 0; s < ST; ++s) issue_pending();
+  {
+    // while the first loads are in flight: tag this warp's share of the
+    // segment arrival counters
+    const long long nctr = static_cast<long long>(B) * Hkv;
+    const long long per = (nctr + W - 1) / W;
+    tag_counters(a.seg_counters, gw * per, min(nctr, (gw + 1) * per), a.epoch, lane);
+  }
 
   // ---- consumer: pieces in order
   Piece cp;
@@ -1106,22 +1138,25 @@ auto dispatch(int head_dim, int block_size, bool fp8, F&& f) -> decltype(f(Inst<
 DecodePlan plan_decode(int batch, int num_heads, int num_kv_heads, int head_dim, int block_size,
                        bool fp8, int len_cap, int num_sms) {
   DecodePlan p{};
-  const size_t slot_floats = static_cast<size_t>(8) * head_dim + 8 * 2;  // one partial slot
   if (batch <= kMaxPersistentBatch) {
     const int per_sm = dispatch(head_dim, block_size, fp8,
                                 [&](auto inst) { return decltype(inst)::ctas_per_sm(); });
     p.persistent_ctas = per_sm * num_sms;
-    p.persistent_slots_per_cta = kWarps;
     p.blocks_per_split = 0;
     p.num_splits = 0;
-    // two partial slots per warp
-    p.workspace_bytes =
-        2 * static_cast<size_t>(p.persistent_ctas) * kWarps * slot_floats * sizeof(float) +
-        (static_cast<size_t>(batch) + 1) * sizeof(int) + 16 +
-        static_cast<size_t>(batch) * num_kv_heads * sizeof(unsigned long long) + 256;
+    // two partial slots per warp, one row per query head of a group (rounded
+    // up to a power of two, the merge's lane layout)
+    p.partial_slots = 2 * static_cast<size_t>(p.persistent_ctas) * kWarps;
+    const int group = std::max(1, num_heads / std::max(1, num_kv_heads));
+    p.slot_rows = group <= 1 ? 1 : group <= 2 ? 2 : group <= 4 ? 4 : 8;
+    const size_t slot_floats = static_cast<size_t>(p.slot_rows) * (head_dim + 2);
+    // partials, prefix sums, 16-byte pad, segment arrival counters
+    p.workspace_bytes = p.partial_slots * slot_floats * sizeof(float) +
+                        (static_cast<size_t>(batch) + 1) * sizeof(int) + 16 +
+                        static_cast<size_t>(batch) * num_kv_heads * sizeof(unsigned long long) +
+                        256;
     return p;
   }
-  (void)num_heads;
   p.persistent_ctas = 0;
   const int max_nblk = (std::max(len_cap, 0) + block_size - 1) / block_size;
   int cb = std::max(1, split_tokens_target() / block_size);
@@ -1132,11 +1167,13 @@ DecodePlan plan_decode(int batch, int num_heads, int num_kv_heads, int head_dim,
     p.blocks_per_split = (max_nblk + 65534) / 65535;
     p.num_splits = (max_nblk + p.blocks_per_split - 1) / p.blocks_per_split;
   }
+  p.slot_rows = 8;
   if (p.num_splits <= 1) {
+    p.partial_slots = 0;
     p.workspace_bytes = 0;
   } else {
-    const size_t slots = static_cast<size_t>(batch) * num_kv_heads * p.num_splits;
-    p.workspace_bytes = slots * slot_floats * sizeof(float) + 256;
+    p.partial_slots = static_cast<size_t>(batch) * num_kv_heads * p.num_splits;
+    p.workspace_bytes = p.partial_slots * 8 * (head_dim + 2) * sizeof(float) + 256;
   }
   return p;
 }

@@ -51,6 +51,7 @@ struct DecodeArgs {
   int* prefix_out;            // persistent path: (B+1) block prefix sums
   unsigned long long* seg_counters;  // persistent path: (B*Hkv) arrival counters
   uint32_t epoch;             // persistent path: tag of this call in seg_counters
+  int slot_rows;              // rows (query heads) of one partial slot
   uint32_t* err;
   // fused append (pa_decode_append): the new token of sequence b, at position
   // context_lens[b]-1, is written to the cache by the warp that attends to it
@@ -72,9 +73,10 @@ struct DecodeArgs {
 // grid-split (blocks per split, number of splits, one slot per split).
 struct DecodePlan {
   int persistent_ctas;
-  int persistent_slots_per_cta;  // warps per CTA: each warp owns 2 partial slots
   int blocks_per_split;
   int num_splits;
+  size_t partial_slots;  // fp32 partials of slot_rows x (head_dim + 2) floats each
+  int slot_rows;
   size_t workspace_bytes;
 };
 
