@@ -33,6 +33,7 @@ _lib = None
 
 KV_BF16 = 0
 KV_E4M3 = 1
+KV_INT8 = 2
 
 _ERRORS = {1: "bad argument", 2: "index or length out of range", 3: "out of memory"}
 
@@ -72,6 +73,9 @@ def _load():
         lib.oracle_decode.restype = i32
         lib.oracle_decode.argtypes = [P, P, P, i32, P, P, i64, i32, i32, i32, P, i32, P, i32, i32,
                                       dbl, P, i32]
+        lib.oracle_decode_window.restype = i32
+        lib.oracle_decode_window.argtypes = [P, P, P, i32, P, P, i64, i32, i32, i32, P, i32, P,
+                                             i32, i32, ctypes.c_double, i64, i64, P, i32]
         lib.oracle_decode_split.restype = i32
         lib.oracle_decode_split.argtypes = [P, P, P, i32, P, P, i64, i32, i32, i32, P, i32, P, i32,
                                             i32, dbl, i32, P]
@@ -140,8 +144,11 @@ def _cache_args(k_cache, v_cache, k_scale, v_scale):
         dtype = KV_BF16
     elif k_cache.dtype == np.uint8:
         dtype = KV_E4M3
+    elif k_cache.dtype == np.int8:
+        dtype = KV_INT8
     else:
-        raise OracleError("cache must hold bf16 bits (uint16) or E4M3 bytes (uint8)")
+        raise OracleError("cache must hold bf16 bits (uint16), E4M3 bytes (uint8) or INT8 "
+                          "codes (int8)")
     kc, vc = np.ascontiguousarray(k_cache), np.ascontiguousarray(v_cache)
     ks = None if k_scale is None else _c(k_scale, np.float32)
     vs = None if v_scale is None else _c(v_scale, np.float32)
@@ -150,11 +157,14 @@ def _cache_args(k_cache, v_cache, k_scale, v_scale):
 
 
 def decode(q, k_cache, v_cache, block_tables, context_lens, scale, k_scale=None, v_scale=None,
-           threads: int | None = None) -> np.ndarray:
+           threads: int | None = None, window: int = 0, sinks: int = 0) -> np.ndarray:
     """Single-query paged decode attention in float64.
 
-    q: (B, H, D) uint16 bf16 bits. Caches (num_blocks, block_size, Hkv, D).
-    block_tables (B, max_blocks) int32; context_lens (B,) int32.
+    q: (B, H, D) uint16 bf16 bits. Caches (num_blocks, block_size, Hkv, D):
+    bf16 bits (uint16), E4M3 bytes (uint8) or INT8 codes (int8), the latter two
+    with scales (num_blocks, Hkv, block_size). block_tables (B, max_blocks)
+    int32; context_lens (B,) int32. window > 0: only the last `window` keys and
+    the first `sinks` keys of each sequence are attended.
     Returns (B, H, D) float64.
     """
     q = _c(q, np.uint16)
@@ -163,8 +173,9 @@ def decode(q, k_cache, v_cache, block_tables, context_lens, scale, k_scale=None,
     keep, cargs = _cache_args(k_cache, v_cache, k_scale, v_scale)
     B, H, D = q.shape
     out = np.zeros((B, H, D), np.float64)
-    _check(_load().oracle_decode(_ptr(q), *cargs, _ptr(bt), bt.shape[1], _ptr(cl), B, H,
-                                 float(scale), _ptr(out), threads or default_threads()))
+    _check(_load().oracle_decode_window(_ptr(q), *cargs, _ptr(bt), bt.shape[1], _ptr(cl), B, H,
+                                        float(scale), int(window), int(sinks), _ptr(out),
+                                        threads or default_threads()))
     del keep
     return out
 

@@ -19,7 +19,9 @@
  *          caveat section: zero-padding to max_len distorts the softmax, so
  *          exactly context_len keys are used.
  *   [GLO]  "Decode Phase" glossary (inferensys.com): q.K^T scores, softmax,
- *          weighted sum of V; FP8 KV-cache quantisation.
+ *          weighted sum of V; FP8 / INT8 KV-cache quantisation; for long
+ *          contexts, sliding window attention (only the most recent W tokens)
+ *          and attention sinks as in StreamingLLM (the initial tokens kept).
  *   [TVL]  "tiny-vllm part 05" (jaehun.me), section "Gathering K/V into a
  *          batched buffer and scattering into blocks": a token at position p
  *          lives in logical block p / BLOCK_SIZE at offset p % BLOCK_SIZE.
@@ -35,7 +37,9 @@
  * cache layout (num_blocks, block_size, num_kv_heads, head_dim) row-major for
  * both K and V; FP8 is OCP E4M3 with one fp32 scale per (slot, kv head) in a
  * (num_blocks, num_kv_heads, block_size) array (one head's scales for one
- * block are contiguous); context_len 0 gives a zero
+ * block are contiguous); INT8 is a signed byte times the same kind of scale
+ * (symmetric, no zero point); a sliding window of W tokens with S sinks
+ * keeps keys p < S and p >= context_len - W; context_len 0 gives a zero
  * output row; a prefill sequence with q_len > kv_len is invalid input.
  */
 #include <math.h>
@@ -47,7 +51,7 @@
 #endif
 
 enum { OR_OK = 0, OR_ERR_ARG = 1, OR_ERR_RANGE = 2, OR_ERR_NOMEM = 3 };
-enum { OR_KV_BF16 = 0, OR_KV_E4M3 = 1 };
+enum { OR_KV_BF16 = 0, OR_KV_E4M3 = 1, OR_KV_INT8 = 2 };
 
 /* bf16 is the upper half of an IEEE binary32; widening is exact. */
 static double bf16_to_double(uint16_t bits) {
@@ -123,14 +127,23 @@ typedef struct {
 } or_cache;
 
 /* Element (slot, kv head, dim) of a cache, widened to double (times the
- * per-(slot, head) scale for E4M3, stored at [block][head][offset]). */
+ * per-(slot, head) scale for E4M3 and INT8, stored at [block][head][offset]). */
 static double cache_elem(const or_cache* c, const void* base, const float* scale,
                          int64_t slot, int g, int dim) {
   int64_t idx = (slot * c->hkv + g) * c->d + dim;
   if (c->dtype == OR_KV_BF16) return bf16_to_double(((const uint16_t*)base)[idx]);
   int64_t block = slot / c->block_size, offset = slot % c->block_size;
   double sc = (double)scale[(block * c->hkv + g) * c->block_size + offset];
+  if (c->dtype == OR_KV_INT8) return (double)((const int8_t*)base)[idx] * sc;
   return oracle_e4m3_to_double(((const uint8_t*)base)[idx]) * sc;
+}
+
+/* Whether key position p is attended by the query of a sequence of n_keys
+ * tokens ([GLO], long-context bullets): with a sliding window (window > 0)
+ * only the last `window` keys and the first `sinks` keys; otherwise all. */
+static int key_visible(int64_t p, int64_t n_keys, int64_t window, int64_t sinks) {
+  if (window <= 0) return 1;
+  return p < sinks || p >= n_keys - window;
 }
 
 /* Slot of logical position p of sequence b, through the block table
@@ -152,12 +165,14 @@ static int64_t slot_of(const or_cache* c, const int32_t* block_tables, int max_b
  * arithmetic, avoids overflow). n_keys == 0 yields a zero row. */
 static int attend_row(const or_cache* c, const int32_t* block_tables, int max_blocks, int b,
                       int g, const uint16_t* qrow, int64_t n_keys, double scale,
-                      double* s /* scratch n_keys */, double* out) {
+                      int64_t window, int64_t sinks, double* s /* scratch n_keys */,
+                      double* out) {
   const int D = c->d;
   for (int dd = 0; dd < D; ++dd) out[dd] = 0.0;
   if (n_keys <= 0) return OR_OK;
   double m = -INFINITY;
   for (int64_t p = 0; p < n_keys; ++p) {
+    if (!key_visible(p, n_keys, window, sinks)) continue;
     int64_t slot = slot_of(c, block_tables, max_blocks, b, p);
     if (slot < 0) return OR_ERR_RANGE;
     double dot = 0.0;
@@ -168,10 +183,12 @@ static int attend_row(const or_cache* c, const int32_t* block_tables, int max_bl
   }
   double l = 0.0;
   for (int64_t p = 0; p < n_keys; ++p) {
+    if (!key_visible(p, n_keys, window, sinks)) continue;
     s[p] = exp(s[p] - m);
     l += s[p];
   }
   for (int64_t p = 0; p < n_keys; ++p) {
+    if (!key_visible(p, n_keys, window, sinks)) continue;
     int64_t slot = slot_of(c, block_tables, max_blocks, b, p);
     double w = s[p] / l;
     for (int dd = 0; dd < D; ++dd)
@@ -183,8 +200,9 @@ static int attend_row(const or_cache* c, const int32_t* block_tables, int max_bl
 static int check_cache(const or_cache* c) {
   if (!c->k_cache || !c->v_cache) return OR_ERR_ARG;
   if (c->block_size <= 0 || c->hkv <= 0 || c->d <= 0 || c->num_blocks <= 0) return OR_ERR_ARG;
-  if (c->dtype != OR_KV_BF16 && c->dtype != OR_KV_E4M3) return OR_ERR_ARG;
-  if (c->dtype == OR_KV_E4M3 && (!c->k_scale || !c->v_scale)) return OR_ERR_ARG;
+  if (c->dtype != OR_KV_BF16 && c->dtype != OR_KV_E4M3 && c->dtype != OR_KV_INT8)
+    return OR_ERR_ARG;
+  if (c->dtype != OR_KV_BF16 && (!c->k_scale || !c->v_scale)) return OR_ERR_ARG;
   return OR_OK;
 }
 
@@ -192,12 +210,14 @@ static int check_cache(const or_cache* c) {
 /* Single-query decode ([DEC] sections 2-4, [GLO]): for every sequence b and
  * query head h, attend over exactly context_lens[b] keys (no padding), using
  * kv head g = h / (num_heads / num_kv_heads). q: (B, H, D) bf16 bits;
- * out: (B, H, D) double. */
-int oracle_decode(const uint16_t* q, const void* k_cache, const void* v_cache, int dtype,
-                  const float* k_scale, const float* v_scale, int64_t num_blocks,
-                  int block_size, int hkv, int d, const int32_t* block_tables, int max_blocks,
-                  const int32_t* context_lens, int batch, int num_heads, double scale,
-                  double* out, int nthreads) {
+ * out: (B, H, D) double. window > 0 restricts the keys to the last `window`
+ * and the first `sinks` positions ([GLO]); window <= 0 attends to all. */
+int oracle_decode_window(const uint16_t* q, const void* k_cache, const void* v_cache,
+                         int dtype, const float* k_scale, const float* v_scale,
+                         int64_t num_blocks, int block_size, int hkv, int d,
+                         const int32_t* block_tables, int max_blocks,
+                         const int32_t* context_lens, int batch, int num_heads, double scale,
+                         int64_t window, int64_t sinks, double* out, int nthreads) {
   or_cache c = {k_cache, v_cache, k_scale, v_scale, dtype, num_blocks, block_size, hkv, d};
   int st = check_cache(&c);
   if (st) return st;
@@ -225,7 +245,7 @@ int oracle_decode(const uint16_t* q, const void* k_cache, const void* v_cache, i
       int b = (int)(r / num_heads), h = (int)(r % num_heads);
       int g = h / group;
       int e = attend_row(&c, block_tables, max_blocks, b, g, q + r * d, context_lens[b], scale,
-                         s, out + r * d);
+                         window, sinks, s, out + r * d);
       if (e) {
 #pragma omp atomic write
         err = e;
@@ -243,6 +263,17 @@ int oracle_decode(const uint16_t* q, const void* k_cache, const void* v_cache, i
  * then M = max_j m_j, l = sum_j l_j exp(m_j - M), o = sum_j o_j exp(m_j - M) / l.
  * This is the online-softmax rescaling that [TVL] describes for
  * pagedAttentionKernel, applied once per chunk. Used to pin the merge step. */
+/* Decode over all context_len keys: the window-free case. */
+int oracle_decode(const uint16_t* q, const void* k_cache, const void* v_cache, int dtype,
+                  const float* k_scale, const float* v_scale, int64_t num_blocks,
+                  int block_size, int hkv, int d, const int32_t* block_tables, int max_blocks,
+                  const int32_t* context_lens, int batch, int num_heads, double scale,
+                  double* out, int nthreads) {
+  return oracle_decode_window(q, k_cache, v_cache, dtype, k_scale, v_scale, num_blocks,
+                              block_size, hkv, d, block_tables, max_blocks, context_lens, batch,
+                              num_heads, scale, 0, 0, out, nthreads);
+}
+
 int oracle_decode_split(const uint16_t* q, const void* k_cache, const void* v_cache, int dtype,
                         const float* k_scale, const float* v_scale, int64_t num_blocks,
                         int block_size, int hkv, int d, const int32_t* block_tables,
@@ -371,7 +402,7 @@ int oracle_prefill(const uint16_t* q, const void* k_cache, const void* v_cache, 
       int64_t cached = kv_len - q_len;
       /* visible keys: j = 0 .. i + cached, i.e. i + cached + 1 of them */
       int e = attend_row(&c, block_tables, max_blocks, b, h / group,
-                         q + (row * num_heads + h) * d, i + cached + 1, scale, s,
+                         q + (row * num_heads + h) * d, i + cached + 1, scale, 0, 0, s,
                          out + (row * num_heads + h) * d);
       if (e) {
 #pragma omp atomic write

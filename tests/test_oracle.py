@@ -288,6 +288,121 @@ def test_fp8_decode_equals_dense_attention_on_dequantised_values():
         np.testing.assert_allclose(got[b], o.numpy(), rtol=0, atol=1e-12)
 
 
+# ---------------------------------------------------------------- window / sinks
+# "Decode Phase" glossary, long-context bullets: a sliding window attends to
+# the most recent W tokens; attention sinks (StreamingLLM) keep the initial
+# tokens as well. Visible keys of a sequence of L tokens: p < S or p >= L - W.
+def _visible(L, window, sinks):
+    if window <= 0:
+        return list(range(L))
+    return [p for p in range(L) if p < sinks or p >= L - window]
+
+
+@pytest.mark.parametrize("window,sinks", [(1, 0), (5, 0), (8, 2), (13, 4), (40, 3), (3, 40),
+                                          (6, 6)])
+def test_window_decode_equals_dense_attention_over_visible_keys(window, sinks):
+    B, H, Hkv, D, bs = 4, 6, 2, 16, 4
+    lens = [1, 9, 17, 38]
+    inp = _with_new(W.make_decode(B, H, Hkv, D, bs, lens, seed=21))
+    got = oracle.decode(_bits(inp.q), _bits(inp.k_cache), _bits(inp.v_cache),
+                        inp.block_tables.numpy(), inp.context_lens.numpy(), inp.scale,
+                        window=window, sinks=sinks)
+    G = H // Hkv
+    for b, L in enumerate(lens):
+        k, v = _dense_kv(inp, b, L)
+        idx = torch.tensor(_visible(L, window, sinks), dtype=torch.long)
+        k = k[idx].repeat_interleave(G, dim=1)
+        v = v[idx].repeat_interleave(G, dim=1)
+        s = torch.einsum("hd,lhd->hl", _f64(inp.q[b]), k) * inp.scale
+        o = torch.einsum("hl,lhd->hd", torch.softmax(s, -1), v)
+        np.testing.assert_allclose(got[b], o.numpy(), rtol=0, atol=1e-12)
+
+
+def test_window_of_one_returns_newest_v_exactly():
+    inp = _with_new(W.make_decode(3, 4, 2, 32, 8, [1, 20, 70], seed=22))
+    got = oracle.decode(_bits(inp.q), _bits(inp.k_cache), _bits(inp.v_cache),
+                        inp.block_tables.numpy(), inp.context_lens.numpy(), inp.scale,
+                        window=1)
+    for b in range(3):
+        np.testing.assert_array_equal(got[b], _f64(inp.v_new[b]).repeat_interleave(2, 0).numpy())
+
+
+def test_window_covering_everything_equals_full_decode():
+    inp = _with_new(W.make_decode(3, 8, 2, 16, 4, [5, 30, 31], seed=23))
+    args = (_bits(inp.q), _bits(inp.k_cache), _bits(inp.v_cache), inp.block_tables.numpy(),
+            inp.context_lens.numpy(), inp.scale)
+    full = oracle.decode(*args)
+    np.testing.assert_array_equal(oracle.decode(*args, window=31), full)
+    np.testing.assert_array_equal(oracle.decode(*args, window=20, sinks=11), full)
+    np.testing.assert_array_equal(oracle.decode(*args, window=0, sinks=3), full)
+
+
+def test_window_equals_full_decode_of_the_visible_tokens_repacked():
+    # the visible keys copied into a fresh, compact cache form a sequence of
+    # their own; full decode over it must give the windowed result
+    B, H, Hkv, D, bs = 3, 4, 2, 16, 4
+    lens = [12, 29, 40]
+    window, sinks = 7, 3
+    inp = _with_new(W.make_decode(B, H, Hkv, D, bs, lens, seed=24))
+    want = oracle.decode(_bits(inp.q), _bits(inp.k_cache), _bits(inp.v_cache),
+                         inp.block_tables.numpy(), inp.context_lens.numpy(), inp.scale,
+                         window=window, sinks=sinks)
+    for b, L in enumerate(lens):
+        vis = _visible(L, window, sinks)
+        n = len(vis)
+        nb = -(-n // bs)
+        kc = torch.zeros((nb, bs, Hkv, D), dtype=torch.bfloat16)
+        vc = torch.zeros_like(kc)
+        for i, p in enumerate(vis):
+            phys = int(inp.block_tables[b, p // bs])
+            kc[i // bs, i % bs] = inp.k_cache[phys, p % bs]
+            vc[i // bs, i % bs] = inp.v_cache[phys, p % bs]
+        bt = np.arange(nb, dtype=np.int32)[None]
+        got = oracle.decode(_bits(inp.q[b:b + 1]), _bits(kc), _bits(vc), bt,
+                            np.array([n], np.int32), inp.scale)
+        np.testing.assert_allclose(got[0], want[b], rtol=0, atol=1e-13)
+
+
+# ---------------------------------------------------------------- INT8 KV
+def test_int8_quantiser_round_trip_bound():
+    g = torch.Generator().manual_seed(25)
+    codes, scales = W._randn_int8((50, 64), g, "cpu")
+    g = torch.Generator().manual_seed(25)
+    x = torch.randn((50, 64), generator=g, dtype=torch.float32).double()
+    c = codes.double()
+    assert c.abs().max() <= 127
+    # the row maximum lands on +-127 exactly; every value within half a step
+    np.testing.assert_array_equal(c.abs().amax(1).numpy(), np.full(50, 127.0))
+    err = (c * scales.double()[:, None] - x).abs()
+    assert bool((err <= scales.double()[:, None] * 0.5 * (1 + 1e-6)).all())
+
+
+def test_int8_decode_equals_dense_attention_on_dequantised_values():
+    B, H, Hkv, D, bs = 3, 8, 2, 32, 8
+    lens = [1, 9, 30]
+    inp = W.make_decode(B, H, Hkv, D, bs, lens, seed=26, kv_dtype="int8")
+    kc, vc = W.u8(inp.k_cache).copy(), W.u8(inp.v_cache).copy()
+    assert kc.dtype == np.int8
+    ksc, vsc = inp.k_scale.numpy().copy(), inp.v_scale.numpy().copy()
+    oracle.store_kv(W.u8(inp.k_new), W.u8(inp.v_new), inp.slot_mapping.numpy(), kc, vc,
+                    inp.k_scale_new.numpy(), inp.v_scale_new.numpy(), ksc, vsc)
+    got = oracle.decode(_bits(inp.q), kc, vc, inp.block_tables.numpy(), inp.context_lens.numpy(),
+                        inp.scale, k_scale=ksc, v_scale=vsc)
+    kd = torch.from_numpy(kc).double() * torch.from_numpy(ksc).double().permute(0, 2, 1)[..., None]
+    vd = torch.from_numpy(vc).double() * torch.from_numpy(vsc).double().permute(0, 2, 1)[..., None]
+    dense = W.DecodeInputs(**{**inp.__dict__, "k_cache": kd, "v_cache": vd})
+    G = H // Hkv
+    for b, L in enumerate(lens):
+        k, v = _dense_kv(dense, b, L)
+        k, v = k.repeat_interleave(G, dim=1), v.repeat_interleave(G, dim=1)
+        s = torch.einsum("hd,lhd->hl", _f64(inp.q[b]), k) * inp.scale
+        o = torch.einsum("hl,lhd->hd", torch.softmax(s, -1), v)
+        np.testing.assert_allclose(got[b], o.numpy(), rtol=0, atol=1e-12)
+    # context_len 1: the newest V row, dequantised, exactly
+    v1 = W.u8(inp.v_new[0]).astype(np.float64) * inp.v_scale_new[0].double().numpy()[:, None]
+    np.testing.assert_array_equal(got[0], np.repeat(v1, G, axis=0))
+
+
 # ---------------------------------------------------------------- prefill
 def _stored_prefill(inp):
     kc, vc = _bits(inp.k_cache).copy(), _bits(inp.v_cache).copy()

@@ -142,6 +142,30 @@ def _randn_fp8(shape, g, device, chunk_rows: int = 1 << 22):
     return codes, scales
 
 
+INT8_MAX = 127.0
+
+
+def _randn_int8(shape, g, device, chunk_rows: int = 1 << 22):
+    """N(0,1) in fp32 quantised to symmetric INT8 with one fp32 scale per row of
+    the last axis: scale = amax / 127 (1 if the row is all zero), code =
+    round-half-to-even(x / scale), in [-127, 127].
+    Returns (codes int8 of `shape`, scales fp32 of shape[:-1])."""
+    codes = torch.empty(shape, dtype=torch.int8, device=device)
+    scales = torch.empty(shape[:-1], dtype=torch.float32, device=device)
+    d = shape[-1]
+    fc = codes.view(-1, d)
+    fs = scales.view(-1)
+    rows = max(1, chunk_rows // d)
+    for r0 in range(0, fc.shape[0], rows):
+        r1 = min(fc.shape[0], r0 + rows)
+        x = torch.randn((r1 - r0, d), generator=g, device=device, dtype=torch.float32)
+        amax = x.abs().amax(dim=1)
+        s = torch.where(amax > 0, amax / INT8_MAX, torch.ones_like(amax))
+        fc[r0:r1] = torch.round(x / s[:, None]).clamp_(-INT8_MAX, INT8_MAX).to(torch.int8)
+        fs[r0:r1] = s
+    return codes, scales
+
+
 def draw_lengths(spec, n: int, g_cpu: torch.Generator) -> list[int]:
     kind = spec[0]
     if kind == "uniform":
@@ -204,6 +228,13 @@ def make_decode(batch: int, num_heads: int, num_kv_heads: int, head_dim: int, bl
         vs = vs.permute(0, 2, 1).contiguous()
         k_new, ksn = _randn_fp8((batch, num_kv_heads, head_dim), g, device)
         v_new, vsn = _randn_fp8((batch, num_kv_heads, head_dim), g, device)
+    elif kv_dtype == "int8":
+        k_cache, ks = _randn_int8(cache_shape, g, device)
+        v_cache, vs = _randn_int8(cache_shape, g, device)
+        ks = ks.permute(0, 2, 1).contiguous()  # (NB, Hkv, bs)
+        vs = vs.permute(0, 2, 1).contiguous()
+        k_new, ksn = _randn_int8((batch, num_kv_heads, head_dim), g, device)
+        v_new, vsn = _randn_int8((batch, num_kv_heads, head_dim), g, device)
     else:
         raise ValueError(kv_dtype)
     q = _randn_bf16((batch, num_heads, head_dim), g, device)
