@@ -41,13 +41,21 @@ METRIC = "Paged decode attention KV-cache GB/s (% of GB300 HBM peak), seq-steps/
 DEFAULT_WORKLOAD = "llama3_8b_decode_b64"
 
 
-def kv_bytes(name: str, lens) -> int:
+def visible_keys(L: int, window: int = 0, sinks: int = 0) -> int:
+    """Keys a query attends to: all L, or with a sliding window the last
+    `window` plus the first `sinks` (counted once where they meet)."""
+    if window <= 0 or L <= window:
+        return L
+    return min(sinks, L - window) + window
+
+
+def kv_bytes(name: str, lens, window: int = 0, sinks: int = 0) -> int:
     w = W.WORKLOADS[name]
     eb = 1 if w["kv_dtype"] == "fp8" else 2
     per_tok = w["num_kv_heads"] * w["head_dim"] * eb * 2
     if w["kv_dtype"] == "fp8":
         per_tok += w["num_kv_heads"] * 4 * 2  # one fp32 scale per (token, head) for K and V
-    return int(sum(lens)) * per_tok
+    return int(sum(visible_keys(L, window, sinks) for L in lens)) * per_tok
 
 
 def _measured(keys):
@@ -209,14 +217,14 @@ def oracle_sample(name: str, max_seqs: int, seed: int = 0):
     return h, lens
 
 
-def run_oracle_step(h, threads: int):
+def run_oracle_step(h, threads: int, window: int = 0, sinks: int = 0):
     import oracle
     if h.kv_dtype == "bf16":
         kc, vc = W.bf16_bits(h.k_cache).copy(), W.bf16_bits(h.v_cache).copy()
         t0 = time.perf_counter()
         oracle.store_kv(W.bf16_bits(h.k_new), W.bf16_bits(h.v_new), h.slot_mapping.numpy(), kc, vc)
         oracle.decode(W.bf16_bits(h.q), kc, vc, h.block_tables.numpy(), h.context_lens.numpy(),
-                      h.scale, threads=threads)
+                      h.scale, threads=threads, window=window, sinks=sinks)
         return time.perf_counter() - t0
     kc, vc = W.u8(h.k_cache).copy(), W.u8(h.v_cache).copy()
     ks, vs = h.k_scale.numpy().copy(), h.v_scale.numpy().copy()
@@ -224,37 +232,40 @@ def run_oracle_step(h, threads: int):
     oracle.store_kv(W.u8(h.k_new), W.u8(h.v_new), h.slot_mapping.numpy(), kc, vc,
                     h.k_scale_new.numpy(), h.v_scale_new.numpy(), ks, vs)
     oracle.decode(W.bf16_bits(h.q), kc, vc, h.block_tables.numpy(), h.context_lens.numpy(),
-                  h.scale, k_scale=ks, v_scale=vs, threads=threads)
+                  h.scale, k_scale=ks, v_scale=vs, threads=threads, window=window, sinks=sinks)
     return time.perf_counter() - t0
 
 
-def sample_size_for(name: str, budget_s: float, threads: int) -> int:
+def sample_size_for(name: str, budget_s: float, threads: int, window: int = 0,
+                    sinks: int = 0) -> int:
     """Sequences per oracle step so one step takes about budget_s (estimated
     from a 1-sequence probe)."""
     h, lens = oracle_sample(name, 1)
-    dt = max(run_oracle_step(h, threads), 1e-4)
-    per_tok = dt / max(1, sum(lens))
+    dt = max(run_oracle_step(h, threads, window, sinks), 1e-4)
+    per_tok = dt / max(1, sum(visible_keys(L, window, sinks) for L in lens))
     all_lens = W.workload_lengths(name)
     n, acc = 0, 0.0
     for L in all_lens:
-        if n > 0 and acc + L * per_tok > budget_s:
+        cost = visible_keys(L, window, sinks) * per_tok
+        if n > 0 and acc + cost > budget_s:
             break
-        acc += L * per_tok
+        acc += cost
         n += 1
     return max(1, n)
 
 
-def cpu_baseline(name: str, budget_s: float = 15.0):
+def cpu_baseline(name: str, budget_s: float = 15.0, window: int = 0, sinks: int = 0):
     import oracle
     oracle.build()
     threads = len(os.sched_getaffinity(0))
-    n = sample_size_for(name, budget_s, threads)
+    n = sample_size_for(name, budget_s, threads, window, sinks)
     h, lens = oracle_sample(name, n)
-    dt = run_oracle_step(h, threads)
-    return {"value": kv_bytes(name, lens) / dt / 1e9, "unit": "GB/s", "cores": threads,
-            "kind": "oracle",
+    dt = run_oracle_step(h, threads, window, sinks)
+    keys = sum(visible_keys(L, window, sinks) for L in lens)
+    return {"value": kv_bytes(name, lens, window, sinks) / dt / 1e9, "unit": "GB/s",
+            "cores": threads, "kind": "oracle",
             "sample": f"first {n} of {len(W.workload_lengths(name))} sequences "
-                      f"({sum(lens)} keys), one store_kv+decode, fp64 C oracle, {dt:.2f} s"}
+                      f"({keys} attended keys), one store_kv+decode, fp64 C oracle, {dt:.2f} s"}
 
 
 def run_reference(args, world, rank):
@@ -265,15 +276,16 @@ def run_reference(args, world, rank):
     oracle.build()
     threads = len(os.sched_getaffinity(0))
     budget = max(0.5, 120.0 / max(1, args.steps + args.warmup))
-    n = sample_size_for(name, budget, threads)
+    win, snk = args.window, args.sinks
+    n = sample_size_for(name, budget, threads, win, snk)
     h, lens = oracle_sample(name, n)
     for _ in range(args.warmup):
-        run_oracle_step(h, threads)
+        run_oracle_step(h, threads, win, snk)
     t = 0.0
     for _ in range(args.steps):
-        t += run_oracle_step(h, threads)
+        t += run_oracle_step(h, threads, win, snk)
     per_step = t / max(1, args.steps)
-    bytes_step = kv_bytes(name, lens)
+    bytes_step = kv_bytes(name, lens, win, snk)
     value = bytes_step / per_step / 1e9
     w = W.WORKLOADS[name]
     line = {
@@ -284,7 +296,8 @@ def run_reference(args, world, rank):
         "config": {"workload": name, "batch": n, "num_heads": w["num_heads"],
                    "num_kv_heads": w["num_kv_heads"], "head_dim": w["head_dim"],
                    "block_size": w["block_size"], "kv_dtype": w["kv_dtype"],
-                   "sample_of_batch": f"{n}/{w['batch']}"},
+                   "sample_of_batch": f"{n}/{w['batch']}",
+                   **({"window": win, "sinks": snk} if win > 0 else {})},
         "seq_steps_per_s": n / per_step,
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle",
                          "sample": f"first {n} of {w['batch']} sequences per step"},
@@ -306,7 +319,8 @@ def run_gpu(args, world, rank, local):
     dev = torch.device("cuda", torch.cuda.current_device())
     lens = W.workload_lengths(name)
     B = w["batch"]
-    step_bytes = kv_bytes(name, lens)
+    win, snk = args.window, args.sinks
+    step_bytes = kv_bytes(name, lens, win, snk)
     pool_bytes = step_bytes
     n_pools = max(2, min(4, math.ceil(4 * L2_BYTES / max(1, pool_bytes)) + 1))
     pools = [W.make_workload(name, device=dev, variant=v + 97 * rank) for v in range(n_pools)]
@@ -319,7 +333,7 @@ def run_gpu(args, world, rank, local):
     out = torch.empty((B, w["num_heads"], w["head_dim"]), dtype=torch.bfloat16, device=dev)
     stream = torch.cuda.current_stream()
 
-    fused = args.step == "append"
+    fused = args.step == "append" and win <= 0  # the fused append has no window variant
 
     def step(p, ev=None):
         if fused:
@@ -336,9 +350,9 @@ def run_gpu(args, world, rank, local):
                     p.v_scale_new, p.k_scale, p.v_scale)
         if ev is not None:
             ev[0].record(stream)
-        pa.decode(p.q, p.k_cache, p.v_cache, p.block_tables, p.context_lens, p.scale,
-                  max_context_len=max_len, out=out, workspace=workspace, k_scale=p.k_scale,
-                  v_scale=p.v_scale)
+        pa.decode_window(p.q, p.k_cache, p.v_cache, p.block_tables, p.context_lens, p.scale,
+                         win, snk, max_context_len=max_len, out=out, workspace=workspace,
+                         k_scale=p.k_scale, v_scale=p.v_scale)
         if ev is not None:
             ev[1].record(stream)
 
@@ -408,9 +422,9 @@ def run_gpu(args, world, rank, local):
         pa.store_kv(dev_in["k_new"], dev_in["v_new"], dev_in["slot_mapping"], p.k_cache,
                     p.v_cache, dev_in.get("k_scale_new"), dev_in.get("v_scale_new"), p.k_scale,
                     p.v_scale)
-        pa.decode(dev_in["q"], p.k_cache, p.v_cache, dev_in["block_tables"],
-                  dev_in["context_lens"], p.scale, max_context_len=max_len, out=out,
-                  workspace=workspace, k_scale=p.k_scale, v_scale=p.v_scale)
+        pa.decode_window(dev_in["q"], p.k_cache, p.v_cache, dev_in["block_tables"],
+                         dev_in["context_lens"], p.scale, win, snk, max_context_len=max_len,
+                         out=out, workspace=workspace, k_scale=p.k_scale, v_scale=p.v_scale)
         out_host.copy_(out, non_blocking=True)
 
     for _ in range(max(3, args.warmup)):
@@ -438,7 +452,7 @@ def run_gpu(args, world, rank, local):
         return
     peak, peak_kind = peaks()
     achieved = step_bytes / (dec_avg_ms / 1e3) / 1e9
-    traffic = traffic_from_profile("pa_decode.cu", name)
+    traffic = traffic_from_profile("pa_decode.cu", name) if win <= 0 else None
     # store_kv + decode (or the fused append: one persistent launch); the
     # grid-split path (batches above 2048) adds a merge
     n_launch = (1 if fused else 2) if B <= 2048 else 3
@@ -453,6 +467,7 @@ def run_gpu(args, world, rank, local):
                    "block_size": w["block_size"], "kv_dtype": w["kv_dtype"],
                    "context_len_mean": sum(lens) / len(lens), "context_len_max": max_len,
                    "kv_bytes_per_step": step_bytes,
+                   **({"window": win, "sinks": snk} if win > 0 else {}),
                    "step": ("decode_append (store of the new tokens fused into decode)"
                             if fused else "store_kv(new tokens) + decode"),
                    "l2": f"rotating {n_pools} KV pools, {n_pools * step_bytes / 1e9:.2f} GB of KV "
@@ -474,7 +489,7 @@ def run_gpu(args, world, rank, local):
         "clocks": clocks,
     }
     if not args.no_cpu_baseline and world == 1:
-        line["cpu_baseline"] = cpu_baseline(name)
+        line["cpu_baseline"] = cpu_baseline(name, window=win, sinks=snk)
     print(json.dumps(line), flush=True)
 
 
@@ -573,6 +588,9 @@ def main():
     ap.add_argument("--impl", choices=["gpu", "reference"], default="gpu")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(W.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--window", type=int, default=0,
+                    help="sliding window in keys (pa_decode_window); 0 = all keys")
+    ap.add_argument("--sinks", type=int, default=0, help="leading keys kept with --window")
     ap.add_argument("--step", choices=["append", "separate"], default="append",
                     help="decode step: fused pa_decode_append, or pa_store_kv + pa_decode")
     args = ap.parse_args()

@@ -13,6 +13,8 @@
  *                      Pass", sections 2-4 and the zero-padding caveat;
  *                      "Decode Phase" glossary, the q.K^T / softmax / sum-of-V
  *                      steps).
+ *   pa_decode_window   pa_decode over a sliding window plus leading sink keys
+ *                      ("Decode Phase" glossary, long-context bullets).
  *   pa_decode_append   pa_store_kv of each sequence's new token followed by
  *                      pa_decode, fused into one persistent kernel.
  *   pa_prefill_varlen  packed varlen prefill over a prefix already in the
@@ -145,6 +147,24 @@ pa_status pa_decode(const void* q, const pa_kv_cache* cache, const int32_t* bloc
                     int32_t max_blocks_per_seq, const int32_t* context_lens,
                     int32_t max_context_len, int32_t batch, int32_t num_heads, float scale,
                     void* out, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * pa_decode_window - pa_decode restricted to a sliding window with attention
+ * sinks ("Decode Phase" glossary, the long-context bullets: sliding window
+ * attention over the most recent W tokens; attention sinks as in
+ * StreamingLLM, keeping the initial tokens). For a sequence of L =
+ * context_len keys the query attends to keys p < sinks and p >= L - window.
+ *   window   > 0: window size in keys; <= 0: all keys (same as pa_decode,
+ *            sinks ignored).
+ *   sinks    >= 0: leading keys always attended (PA_ERR_SHAPE if negative).
+ *   other arguments as pa_decode (same workspace size). Blocks that hold no
+ *   visible key are not read. Batches above 2048 return PA_ERR_UNSUPPORTED.
+ */
+pa_status pa_decode_window(const void* q, const pa_kv_cache* cache, const int32_t* block_tables,
+                           int32_t max_blocks_per_seq, const int32_t* context_lens,
+                           int32_t max_context_len, int32_t batch, int32_t num_heads,
+                           float scale, int32_t window, int32_t sinks, void* out, void* workspace,
+                           size_t workspace_bytes, void* stream);
 
 /*
  * pa_decode_append - one decode step's store and attention in one call: the

@@ -35,8 +35,8 @@ DECODE_NOALLOC_SCRATCH_BYTES = 32 << 20
 
 # Every symbol include/pa.h declares.
 EXPORTED = ("pa_abi_version", "pa_status_string", "pa_store_kv", "pa_decode_workspace_size",
-            "pa_decode", "pa_decode_append", "pa_prefill_varlen", "pa_decode_noalloc",
-            "pa_get_device_error")
+            "pa_decode", "pa_decode_window", "pa_decode_append", "pa_prefill_varlen",
+            "pa_decode_noalloc", "pa_get_device_error")
 
 
 class PAError(RuntimeError):
@@ -78,6 +78,9 @@ def lib() -> ctypes.CDLL:
     L.pa_decode.restype = ctypes.c_int
     L.pa_decode.argtypes = [P, ctypes.POINTER(KVCache), P, i32, P, i32, i32, i32, ctypes.c_float,
                             P, P, ctypes.c_size_t, P]
+    L.pa_decode_window.restype = ctypes.c_int
+    L.pa_decode_window.argtypes = [P, ctypes.POINTER(KVCache), P, i32, P, i32, i32, i32,
+                                   ctypes.c_float, i32, i32, P, P, ctypes.c_size_t, P]
     L.pa_decode_append.restype = ctypes.c_int
     L.pa_decode_append.argtypes = [P, P, P, P, P, ctypes.POINTER(KVCache), P, i32, P, i32, i32,
                                    i32, ctypes.c_float, P, P, ctypes.c_size_t, P]
@@ -167,6 +170,30 @@ def decode(q, k_cache, v_cache, block_tables, context_lens, scale: float, *,
     _check(lib().pa_decode(_ptr(q.contiguous()), ctypes.byref(cache), _ptr(bt), bt.shape[1],
                            _ptr(cl), int(max_context_len), B, H, float(scale), _ptr(out),
                            _ptr(workspace), ws_bytes, _stream()), "pa_decode")
+    return out
+
+
+def decode_window(q, k_cache, v_cache, block_tables, context_lens, scale: float, window: int,
+                  sinks: int = 0, *, max_context_len: int = 0, out=None, workspace=None,
+                  k_scale=None, v_scale=None) -> torch.Tensor:
+    """pa_decode_window: decode attention over the last `window` keys and the
+    first `sinks` keys of each sequence (window <= 0: all keys)."""
+    cache = make_cache(k_cache, v_cache, k_scale, v_scale)
+    B, H, D = q.shape
+    bt = block_tables.contiguous()
+    cl = context_lens.contiguous()
+    if out is None:
+        out = torch.empty((B, H, D), dtype=torch.bfloat16, device=q.device)
+    if workspace is None:
+        need = int(lib().pa_decode_workspace_size(ctypes.byref(cache), B, H, bt.shape[1],
+                                                  max_context_len))
+        if need:
+            workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().pa_decode_window(_ptr(q.contiguous()), ctypes.byref(cache), _ptr(bt),
+                                  bt.shape[1], _ptr(cl), int(max_context_len), B, H, float(scale),
+                                  int(window), int(sinks), _ptr(out), _ptr(workspace), ws_bytes,
+                                  _stream()), "pa_decode_window")
     return out
 
 

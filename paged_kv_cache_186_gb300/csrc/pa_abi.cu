@@ -235,9 +235,10 @@ pa_status decode_common(const void* q, const pa_kv_cache* cache, const int32_t* 
                         int32_t max_context_len, int32_t batch, int32_t num_heads, float scale,
                         void* out, void* workspace, size_t workspace_bytes, void* stream,
                         const void* k_new, const void* v_new, const float* k_scale_new,
-                        const float* v_scale_new) {
+                        const float* v_scale_new, int32_t window, int32_t sinks) {
   pa_status st = check_cache(cache);
   if (st != PA_OK) return st;
+  if (sinks < 0) return PA_ERR_SHAPE;
   if (batch < 0 || num_heads <= 0 || max_blocks_per_seq <= 0) return PA_ERR_SHAPE;
   if (batch == 0) return PA_OK;
   if (q == nullptr || block_tables == nullptr || context_lens == nullptr || out == nullptr)
@@ -258,6 +259,7 @@ pa_status decode_common(const void* q, const pa_kv_cache* cache, const int32_t* 
   if (plan.workspace_bytes > 0 &&
       (workspace == nullptr || workspace_bytes < plan.workspace_bytes || !aligned16(workspace)))
     return PA_ERR_WORKSPACE;
+  if (window > 0 && plan.persistent_ctas == 0) return PA_ERR_UNSUPPORTED;
   CUtensorMap kmap, vmap;
   if ((st = cached_cache_map(&kmap, cache->k_cache, cache)) != PA_OK) return st;
   if ((st = cached_cache_map(&vmap, cache->v_cache, cache)) != PA_OK) return st;
@@ -320,6 +322,8 @@ pa_status decode_common(const void* q, const pa_kv_cache* cache, const int32_t* 
   a.max_blocks = max_blocks_per_seq;
   a.num_blocks = cache->num_blocks;
   a.len_cap = cap;
+  a.window = window > 0 ? window : 0;
+  a.sinks = window > 0 ? sinks : 0;
   a.persistent_ctas = plan.persistent_ctas;
   a.blocks_per_split = plan.blocks_per_split;
   a.num_splits = plan.num_splits;
@@ -338,7 +342,17 @@ pa_status pa_decode(const void* q, const pa_kv_cache* cache, const int32_t* bloc
                     void* out, void* workspace, size_t workspace_bytes, void* stream) {
   return decode_common(q, cache, block_tables, max_blocks_per_seq, context_lens, max_context_len,
                        batch, num_heads, scale, out, workspace, workspace_bytes, stream, nullptr,
-                       nullptr, nullptr, nullptr);
+                       nullptr, nullptr, nullptr, 0, 0);
+}
+
+pa_status pa_decode_window(const void* q, const pa_kv_cache* cache, const int32_t* block_tables,
+                           int32_t max_blocks_per_seq, const int32_t* context_lens,
+                           int32_t max_context_len, int32_t batch, int32_t num_heads,
+                           float scale, int32_t window, int32_t sinks, void* out, void* workspace,
+                           size_t workspace_bytes, void* stream) {
+  return decode_common(q, cache, block_tables, max_blocks_per_seq, context_lens, max_context_len,
+                       batch, num_heads, scale, out, workspace, workspace_bytes, stream, nullptr,
+                       nullptr, nullptr, nullptr, window, sinks);
 }
 
 pa_status pa_decode_append(const void* q, const void* k_new, const void* v_new,
@@ -356,7 +370,7 @@ pa_status pa_decode_append(const void* q, const void* k_new, const void* v_new,
   if (batch > 0 && (!aligned16(k_new) || !aligned16(v_new))) return PA_ERR_ALIGN;
   return decode_common(q, cache, block_tables, max_blocks_per_seq, context_lens, max_context_len,
                        batch, num_heads, scale, out, workspace, workspace_bytes, stream, k_new,
-                       v_new, k_scale_new, v_scale_new);
+                       v_new, k_scale_new, v_scale_new, 0, 0);
 }
 
 pa_status pa_prefill_varlen(const void* q, const pa_kv_cache* cache, const int32_t* block_tables,

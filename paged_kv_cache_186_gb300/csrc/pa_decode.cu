@@ -110,16 +110,19 @@ __device__ __forceinline__ void load_q(const DecodeArgs& a, int b, int kvh, int 
 // lane group r; acc = O^T fragments for heads 2q4, 2q4+1). The whole block is
 // one softmax step: S for its BS tokens (BS/8 n-tiles, independent MMA
 // chains), one max/sum update, then P.V per 16-token group.
-template <int D, int BS, bool FP8>
+template <int D, int BS, bool FP8, bool HOLE = false>
 __device__ __forceinline__ void attend_block(uint32_t kt, uint32_t vt, const uint8_t* base_ptr,
                                              uint32_t base, const float* ksc, const float* vsc,
-                                             int tok0, int L, const uint32_t (&qa)[D / 16][2],
+                                             int tok0, int L, int hole_lo, int hole_hi,
+                                             const uint32_t (&qa)[D / 16][2],
                                              float (&acc)[D / 16][4], float& m_run, float& l_run,
                                              float sl2, int lane) {
   constexpr int NT = BS / 8;  // n-tiles of 8 tokens
   constexpr int NG = BS / 16;  // 16-token groups (k-steps of P.V)
   const int r = lane >> 2, q4 = lane & 3;
-  const bool partial = tok0 + BS > L;
+  // keys t < L outside the window's hole [hole_lo, hole_hi) take part
+  auto valid = [&](int t) { return t < L && (!HOLE || t < hole_lo || t >= hole_hi); };
+  const bool partial = tok0 + BS > L || (HOLE && hole_lo < tok0 + BS && hole_hi > tok0);
   // ---- S = Q K^T for the block's tokens
   float sc[NT][4];
 #pragma unroll
@@ -174,7 +177,7 @@ __device__ __forceinline__ void attend_block(uint32_t kt, uint32_t vt, const uin
   if (partial) {
 #pragma unroll
     for (int j = 0; j < 2 * NT; ++j)
-      if (tok0 + (j >> 1) * 8 + 2 * q4 + (j & 1) >= L) x[j] = -INFINITY;
+      if (!valid(tok0 + (j >> 1) * 8 + 2 * q4 + (j & 1))) x[j] = -INFINITY;
   }
   float mx = x[0];
 #pragma unroll
@@ -211,9 +214,9 @@ __device__ __forceinline__ void attend_block(uint32_t kt, uint32_t vt, const uin
     const int g0 = tok0 + hg * 16 + 2 * q4;  // tokens of this lane's P entries: g0, g0+1, g0+8, g0+9
     if (partial && hg * 16 + tok0 >= L) break;
     uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;
-    if (partial) {  // V rows past the sequence may hold anything: zero their fragments
-      mlo = (g0 < L ? 0x0000ffffu : 0u) | (g0 + 1 < L ? 0xffff0000u : 0u);
-      mhi = (g0 + 8 < L ? 0x0000ffffu : 0u) | (g0 + 9 < L ? 0xffff0000u : 0u);
+    if (partial) {  // V rows of masked keys may hold anything: zero their fragments
+      mlo = (valid(g0) ? 0x0000ffffu : 0u) | (valid(g0 + 1) ? 0xffff0000u : 0u);
+      mhi = (valid(g0 + 8) ? 0x0000ffffu : 0u) | (valid(g0 + 9) ? 0xffff0000u : 0u);
     }
     const float p0 = pr[4 * hg], p1 = pr[4 * hg + 1], p8 = pr[4 * hg + 2], p9 = pr[4 * hg + 3];
     if constexpr (!FP8) {
@@ -240,8 +243,9 @@ __device__ __forceinline__ void attend_block(uint32_t kt, uint32_t vt, const uin
       const float2 v0 = *reinterpret_cast<const float2*>(vsc + hg * 16 + 2 * q4);
       const float2 v1 = *reinterpret_cast<const float2*>(vsc + hg * 16 + 8 + 2 * q4);
       // masked tokens have p = 0 but their scales may be anything: select, not multiply
-      const uint32_t pb0 = pack_f16x2(g0 < L ? p0 * v0.x : 0.f, g0 + 1 < L ? p1 * v0.y : 0.f);
-      const uint32_t pb1 = pack_f16x2(g0 + 8 < L ? p8 * v1.x : 0.f, g0 + 9 < L ? p9 * v1.y : 0.f);
+      const uint32_t pb0 = pack_f16x2(valid(g0) ? p0 * v0.x : 0.f, valid(g0 + 1) ? p1 * v0.y : 0.f);
+      const uint32_t pb1 =
+          pack_f16x2(valid(g0 + 8) ? p8 * v1.x : 0.f, valid(g0 + 9) ? p9 * v1.y : 0.f);
       // lane (r, q4) reads 16-byte chunk r of token rows 2q4, 2q4+1, 2q4+8, 2q4+9:
       // word w gives dims 16r + 4w + {0..3}; output row mapping in the writers.
       const int t0 = hg * 16 + 2 * q4;
@@ -342,6 +346,40 @@ __device__ __forceinline__ void merge_warps_and_write(const float* mo, const Dec
       }
     }
   }
+}
+
+// Sliding window with sinks: blocks of a sequence of L keys that hold a
+// visible key (p < sinks or p >= L - window). They are the first `sb` blocks
+// and the blocks from `sb + shift` on, so visible block v is logical block
+// v < sb ? v : v + shift; the hole of invisible keys is [hole_lo, hole_hi).
+// window <= 0 (or a window reaching back to the sinks) keeps every block.
+struct SeqWindow {
+  int nvis, sb, shift, hole_lo, hole_hi;
+  __device__ __forceinline__ int logical(int v) const { return v < sb ? v : v + shift; }
+};
+
+template <int BS>
+__device__ __forceinline__ SeqWindow seq_window(int L, int window, int sinks) {
+  SeqWindow w;
+  const int nblk = (L + BS - 1) / BS;
+  w.nvis = nblk;
+  w.sb = nblk;
+  w.shift = 0;
+  w.hole_lo = w.hole_hi = 0;
+  if (window > 0 && L > window) {
+    const int se = min(sinks, L), lo = L - window;
+    if (se < lo) {
+      w.hole_lo = se;
+      w.hole_hi = lo;
+      const int sb = (se + BS - 1) / BS, wb0 = lo / BS;
+      if (wb0 > sb) {
+        w.sb = sb;
+        w.shift = wb0 - sb;
+        w.nvis = sb + (nblk - wb0);
+      }
+    }
+  }
+  return w;
 }
 
 // ============================================================ persistent path
@@ -661,7 +699,7 @@ __device__ __noinline__ void append_row(uint8_t* tile, float* stage_scales, cons
   __syncwarp();
 }
 
-template <int D, int BS, int NW, int ST, bool FP8>
+template <int D, int BS, int NW, int ST, bool FP8, bool WIN>
 __global__ void __launch_bounds__(NW * 32, 3)
     decode_persistent_kernel(const __grid_constant__ CUtensorMap kmap,
                              const __grid_constant__ CUtensorMap vmap, const DecodeArgs a) {
@@ -690,7 +728,9 @@ __global__ void __launch_bounds__(NW * 32, 3)
   for (int base_i = 0; base_i < B; base_i += NW * 32) {
     const int i = base_i + threadIdx.x;
     int v = 0;
-    if (i < B) v = (min(max(a.context_lens[i], 0), a.len_cap) + BS - 1) / BS;
+    if (i < B)
+      v = seq_window<BS>(min(max(a.context_lens[i], 0), a.len_cap), WIN ? a.window : 0, a.sinks)
+              .nvis;
     int incl = v;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -759,7 +799,11 @@ __global__ void __launch_bounds__(NW * 32, 3)
       const int nb = prefix[lo + 1] - prefix[lo];
       const long long off = r - static_cast<long long>(prefix[lo]) * Hkv;
       kvh_o = static_cast<int>(off / nb);
-      phys_o = a.block_tables[static_cast<long long>(lo) * a.max_blocks + off % nb];
+      int blk = static_cast<int>(off % nb);
+      if (WIN)
+        blk = seq_window<BS>(min(max(a.context_lens[lo], 0), a.len_cap), a.window, a.sinks)
+                  .logical(blk);
+      phys_o = a.block_tables[static_cast<long long>(lo) * a.max_blocks + blk];
     }
   };
   int cur_kvh, cur_phys, nxt_kvh, nxt_phys;
@@ -822,11 +866,13 @@ __global__ void __launch_bounds__(NW * 32, 3)
     uint32_t qa[D / 16][2];
     load_q<D, FP8>(a, cp.b, cp.kvh, lane, qa);
     const int L = min(max(a.context_lens[cp.b], 0), a.len_cap);
+    const SeqWindow sw = seq_window<BS>(L, WIN ? a.window : 0, a.sinks);
     float acc[D / 16][4];
 #pragma unroll
     for (int mt = 0; mt < D / 16; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
     float m_run = -INFINITY, l_run = 0.f;
-    for (int blk = cp.lo; blk < cp.hi; ++blk) {
+    for (int vb = cp.lo; vb < cp.hi; ++vb) {
+      const int blk = sw.logical(vb);  // visible block -> logical block
       const int s = consumed % ST;
       const bool got = mbar_wait(bar0 + 8 * s, (consumed / ST) & 1);
       if (!__all_sync(kFull, got)) {
@@ -836,13 +882,13 @@ __global__ void __launch_bounds__(NW * 32, 3)
       }
       const uint32_t kt = stage0 + s * C::kStage;
       const float* ksc = scale_ptr + ((warp * ST + s) * 2) * BS;
-      if (a.k_new != nullptr && blk == cp.nblk - 1)
+      if (a.k_new != nullptr && vb == cp.nblk - 1)
         append_row<D, BS, FP8>(base_ptr + (kt - base),
                                const_cast<float*>(scale_ptr) + ((warp * ST + s) * 2) * BS,
                                a.block_tables + static_cast<long long>(cp.b) * a.max_blocks + blk,
                                cp.b * Hkv + cp.kvh, (L - 1) - blk * BS, a, lane);
-      attend_block<D, BS, FP8>(kt, kt + C::kTile, base_ptr, base, ksc, ksc + BS, blk * BS, L, qa,
-                               acc, m_run, l_run, sl2, lane);
+      attend_block<D, BS, FP8, WIN>(kt, kt + C::kTile, base_ptr, base, ksc, ksc + BS, blk * BS, L,
+                                    sw.hole_lo, sw.hole_hi, qa, acc, m_run, l_run, sl2, lane);
       ++consumed;
       __syncwarp();
       issue_pending();
@@ -968,8 +1014,8 @@ __global__ void __launch_bounds__(NW * 32)
     const uint32_t kt = stage0 + s * C::kStage;
     const float* ksc = scale_ptr + ((warp * ST + s) * 2) * BS;
     attend_block<D, BS, FP8>(kt, kt + C::kTile, base_ptr, base, ksc, ksc + BS,
-                             (blk0 + warp + i * NW) * BS, L, qa, acc, m_run, l_run, a.scale_log2,
-                             lane);
+                             (blk0 + warp + i * NW) * BS, L, 0, 0, qa, acc, m_run, l_run,
+                             a.scale_log2, lane);
     __syncwarp();
     if (i + ST < n_my) issue(i + ST);
   }
@@ -1063,13 +1109,20 @@ struct Inst {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 1;
     if (cached[dev] > 0) return cached[dev];
-    auto* k = decode_persistent_kernel<D, BS, kWarps, kStages, FP8>;
+    // both variants (with and without a sliding window) get the attribute;
+    // the grid is sized by the one with fewer resident CTAs
+    auto* k0 = decode_persistent_kernel<D, BS, kWarps, kStages, FP8, false>;
+    auto* k1 = decode_persistent_kernel<D, BS, kWarps, kStages, FP8, true>;
     const int smem = PC::smem_bytes(kMaxPersistentBatch);
-    int n = 0;
-    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, kWarps * 32, smem) != cudaSuccess)
+    int n0 = 0, n1 = 0;
+    if (cudaFuncSetAttribute(k0, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+            cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n0, k0, kWarps * 32, smem) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n1, k1, kWarps * 32, smem) != cudaSuccess)
       return 1;
-    cached[dev] = std::max(1, n);
+    cached[dev] = std::max(1, std::min(n0, n1));
     return cached[dev];
   }
 
@@ -1078,7 +1131,8 @@ struct Inst {
     cudaError_t e;
     const long long rows = static_cast<long long>(a.batch) * a.num_heads;
     if (a.persistent_ctas > 0) {
-      auto* k = decode_persistent_kernel<D, BS, kWarps, kStages, FP8>;
+      auto* k = a.window > 0 ? decode_persistent_kernel<D, BS, kWarps, kStages, FP8, true>
+                             : decode_persistent_kernel<D, BS, kWarps, kStages, FP8, false>;
       (void)ctas_per_sm();  // makes sure the shared-memory attribute is set on this device
       // programmatic dependent launch: the prologue may overlap the kernel
       // before this one on the stream (the kernel waits before reading K/V)

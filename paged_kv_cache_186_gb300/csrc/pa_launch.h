@@ -63,6 +63,7 @@ struct DecodeArgs {
   void* v_cache;
   int batch, num_heads, num_kv_heads, group, head_dim, block_size;
   int max_blocks, num_blocks, len_cap;
+  int window, sinks;          // sliding window (> 0) with leading sink keys; 0 = all keys
   int persistent_ctas;        // > 0: persistent kernel with this many CTAs
   int blocks_per_split, num_splits;  // grid-split path
   bool fp8;
