@@ -51,9 +51,10 @@ def visible_keys(L: int, window: int = 0, sinks: int = 0) -> int:
 
 def kv_bytes(name: str, lens, window: int = 0, sinks: int = 0) -> int:
     w = W.WORKLOADS[name]
-    eb = 1 if w["kv_dtype"] == "fp8" else 2
+    q8 = w["kv_dtype"] in ("fp8", "int8")
+    eb = 1 if q8 else 2
     per_tok = w["num_kv_heads"] * w["head_dim"] * eb * 2
-    if w["kv_dtype"] == "fp8":
+    if q8:
         per_tok += w["num_kv_heads"] * 4 * 2  # one fp32 scale per (token, head) for K and V
     return int(sum(visible_keys(L, window, sinks) for L in lens)) * per_tok
 
@@ -324,7 +325,7 @@ def run_gpu(args, world, rank, local):
     pool_bytes = step_bytes
     n_pools = max(2, min(4, math.ceil(4 * L2_BYTES / max(1, pool_bytes)) + 1))
     pools = [W.make_workload(name, device=dev, variant=v + 97 * rank) for v in range(n_pools)]
-    fp8 = w["kv_dtype"] == "fp8"
+    q8 = w["kv_dtype"] in ("fp8", "int8")  # 8-bit codes with scales
     max_len = max(lens)
     ws_bytes = pa.decode_workspace_size(pools[0].k_cache, B, w["num_heads"],
                                         pools[0].block_tables.shape[1], max_len,
@@ -399,7 +400,7 @@ def run_gpu(args, world, rank, local):
     if not fused:
         host_keys += ("slot_mapping",)
     host = {k: getattr(p0, k).cpu().pin_memory() for k in host_keys}
-    if fp8:
+    if q8:
         host["k_scale_new"] = p0.k_scale_new.cpu().pin_memory()
         host["v_scale_new"] = p0.v_scale_new.cpu().pin_memory()
     dev_in = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
@@ -461,7 +462,8 @@ def run_gpu(args, world, rank, local):
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_total / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "fp8_e4m3" if fp8 else "bf16", "data": "synthetic",
+        "dtype": {"fp8": "fp8_e4m3", "int8": "int8"}.get(w["kv_dtype"], "bf16"),
+        "data": "synthetic",
         "config": {"workload": name, "batch": B, "num_heads": w["num_heads"],
                    "num_kv_heads": w["num_kv_heads"], "head_dim": w["head_dim"],
                    "block_size": w["block_size"], "kv_dtype": w["kv_dtype"],

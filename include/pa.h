@@ -35,15 +35,17 @@
  *     pa_get_device_error().
  *   - Layouts (row-major, contiguous):
  *       k_cache, v_cache  (num_blocks, block_size, num_kv_heads, head_dim)
- *                         bf16, or FP8-E4M3 bytes (OCP "e4m3fn");
- *       k_scale, v_scale  (num_blocks, num_kv_heads, block_size) fp32, FP8
- *                         only: element = code value * scale;
+ *                         bf16, FP8-E4M3 bytes (OCP "e4m3fn") or signed INT8
+ *                         codes (the "Decode Phase" glossary names FP8 and
+ *                         INT8 KV-cache quantisation);
+ *       k_scale, v_scale  (num_blocks, num_kv_heads, block_size) fp32, 8-bit
+ *                         caches only: element = code value * scale;
  *       block_tables      (batch, max_blocks_per_seq) int32, physical block
  *                         of logical block j of sequence b;
  *       slot              physical_block * block_size + offset (int64).
  *   - Head map (GQA/MQA): query head h reads kv head h / (num_heads /
  *     num_kv_heads), i.e. the repeat_interleave grouping of the decode page.
- *   - Supported: head_dim 64 or 128 (FP8: 128), block_size 16 or 32,
+ *   - Supported: head_dim 64 or 128 (8-bit caches: 128), block_size 16 or 32,
  *     num_heads a multiple of num_kv_heads with at most 8 query heads per kv
  *     head. Anything else returns PA_ERR_UNSUPPORTED.
  */
@@ -72,7 +74,7 @@ typedef enum {
                              library's static buffer holds */
 } pa_status;
 
-typedef enum { PA_KV_BF16 = 0, PA_KV_FP8_E4M3 = 1 } pa_kv_dtype;
+typedef enum { PA_KV_BF16 = 0, PA_KV_FP8_E4M3 = 1, PA_KV_INT8 = 2 } pa_kv_dtype;
 
 /* Device error word bits (pa_get_device_error). */
 #define PA_DEVERR_SLOT_RANGE 0x1u   /* store_kv: slot >= num_blocks*block_size, skipped */
@@ -89,7 +91,7 @@ typedef struct {
   int32_t dtype;        /* pa_kv_dtype */
   void* k_cache;        /* (num_blocks, block_size, num_kv_heads, head_dim) */
   void* v_cache;
-  float* k_scale;       /* (num_blocks, num_kv_heads, block_size), FP8 only, else NULL */
+  float* k_scale;       /* (num_blocks, num_kv_heads, block_size), 8-bit only, else NULL */
   float* v_scale;
 } pa_kv_cache;
 
@@ -102,8 +104,8 @@ const char* pa_status_string(pa_status status);
 /*
  * pa_store_kv - write num_tokens new K/V rows into the cache.
  *   k, v           (num_tokens, num_kv_heads, head_dim), cache dtype (bf16, or
- *                  E4M3 bytes for an FP8 cache), device.
- *   k_scale_new,   (num_tokens, num_kv_heads) fp32, FP8 caches only (else NULL).
+ *                  E4M3 / INT8 bytes for an 8-bit cache), device.
+ *   k_scale_new,   (num_tokens, num_kv_heads) fp32, 8-bit caches only (else NULL).
  *   v_scale_new
  *   slot_mapping   (num_tokens) int64: destination slot of token t; a negative
  *                  slot skips the token (padding). Slots within one call must
@@ -140,7 +142,7 @@ size_t pa_decode_workspace_size(const pa_kv_cache* cache, int32_t batch, int32_t
  *   workspace       device scratch of at least pa_decode_workspace_size()
  *                   bytes (may be NULL when that is 0). Contents on entry are
  *                   ignored; calls sharing one workspace must not overlap.
- * Arithmetic: bf16 (or E4M3 widened exactly to f16) operands, fp32 scores,
+ * Arithmetic: bf16 (or E4M3 / INT8 codes widened exactly to f16) operands, fp32 scores,
  * softmax and accumulation, one round to bf16 at the output.
  */
 pa_status pa_decode(const void* q, const pa_kv_cache* cache, const int32_t* block_tables,
@@ -173,7 +175,7 @@ pa_status pa_decode_window(const void* q, const pa_kv_cache* cache, const int32_
  * Attention Forward Pass", section 2, the store-then-attend order).
  *   k_new, v_new    (batch, num_kv_heads, head_dim), cache dtype, device,
  *                   16-byte aligned: the new token of sequence b.
- *   k_scale_new,    (batch, num_kv_heads) fp32, FP8 caches only (else NULL).
+ *   k_scale_new,    (batch, num_kv_heads) fp32, 8-bit caches only (else NULL).
  *   v_scale_new
  *   other arguments as pa_decode (same workspace size).
  * The row goes to position p = min(context_len, bound) - 1 of its sequence,

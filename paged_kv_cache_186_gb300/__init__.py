@@ -21,6 +21,7 @@ LIB_PATH = os.path.join(_PKG, "libpa_gb300.so")
 
 PA_KV_BF16 = 0
 PA_KV_FP8_E4M3 = 1
+PA_KV_INT8 = 2
 
 PA_DEVERR_SLOT_RANGE = 0x1
 PA_DEVERR_WAIT_TIMEOUT = 0x2
@@ -113,11 +114,14 @@ def _check(code: int, what: str):
 def make_cache(k_cache: torch.Tensor, v_cache: torch.Tensor, k_scale: torch.Tensor | None = None,
                v_scale: torch.Tensor | None = None) -> KVCache:
     """Describe caches of shape (num_blocks, block_size, num_kv_heads, head_dim):
-    bf16, or uint8 E4M3 codes with fp32 scales (num_blocks, num_kv_heads, block_size)."""
+    bf16, or uint8 E4M3 / int8 codes with fp32 scales (num_blocks, num_kv_heads,
+    block_size)."""
     if k_cache.dtype == torch.bfloat16:
         dt = PA_KV_BF16
     elif k_cache.dtype in (torch.uint8, torch.float8_e4m3fn):
         dt = PA_KV_FP8_E4M3
+    elif k_cache.dtype == torch.int8:
+        dt = PA_KV_INT8
     else:
         raise TypeError(f"unsupported cache dtype {k_cache.dtype}")
     for t in (k_cache, v_cache, k_scale, v_scale):

@@ -71,20 +71,21 @@ pa_status check_cache(const pa_kv_cache* c) {
   if (c == nullptr || c->k_cache == nullptr || c->v_cache == nullptr) return PA_ERR_NULL;
   if (c->num_blocks <= 0 || c->block_size <= 0 || c->num_kv_heads <= 0 || c->head_dim <= 0)
     return PA_ERR_SHAPE;
-  if (c->dtype != PA_KV_BF16 && c->dtype != PA_KV_FP8_E4M3) return PA_ERR_DTYPE;
-  const bool fp8 = c->dtype == PA_KV_FP8_E4M3;
-  if (fp8 && (c->k_scale == nullptr || c->v_scale == nullptr)) return PA_ERR_DTYPE;
-  if (!fp8 && (c->k_scale != nullptr || c->v_scale != nullptr)) return PA_ERR_DTYPE;
+  if (c->dtype != PA_KV_BF16 && c->dtype != PA_KV_FP8_E4M3 && c->dtype != PA_KV_INT8)
+    return PA_ERR_DTYPE;
+  const bool q8 = c->dtype != PA_KV_BF16;  // 8-bit codes with scales
+  if (q8 && (c->k_scale == nullptr || c->v_scale == nullptr)) return PA_ERR_DTYPE;
+  if (!q8 && (c->k_scale != nullptr || c->v_scale != nullptr)) return PA_ERR_DTYPE;
   if (c->block_size != 16 && c->block_size != 32) return PA_ERR_UNSUPPORTED;
-  if (fp8 ? c->head_dim != 128 : (c->head_dim != 64 && c->head_dim != 128))
+  if (q8 ? c->head_dim != 128 : (c->head_dim != 64 && c->head_dim != 128))
     return PA_ERR_UNSUPPORTED;
   if (static_cast<long long>(c->num_blocks) * c->block_size > 0x7fffffffLL) return PA_ERR_SHAPE;
   if (!aligned16(c->k_cache) || !aligned16(c->v_cache)) return PA_ERR_ALIGN;
-  if (fp8 && (!aligned16(c->k_scale) || !aligned16(c->v_scale))) return PA_ERR_ALIGN;
+  if (q8 && (!aligned16(c->k_scale) || !aligned16(c->v_scale))) return PA_ERR_ALIGN;
   return PA_OK;
 }
 
-int elem_bytes(const pa_kv_cache* c) { return c->dtype == PA_KV_FP8_E4M3 ? 1 : 2; }
+int elem_bytes(const pa_kv_cache* c) { return c->dtype == PA_KV_BF16 ? 2 : 1; }
 
 // Tensor map over a cache viewed as 3-D (head_dim, num_kv_heads,
 // num_blocks*block_size), boxes of one 128-byte-wide, block_size-tall tile of
@@ -188,8 +189,8 @@ pa_status pa_store_kv(const void* k, const void* v, const float* k_scale_new,
   if (num_tokens < 0) return PA_ERR_SHAPE;
   if (num_tokens == 0) return PA_OK;
   if (k == nullptr || v == nullptr || slot_mapping == nullptr) return PA_ERR_NULL;
-  const bool fp8 = cache->dtype == PA_KV_FP8_E4M3;
-  if (fp8 != (k_scale_new != nullptr) || fp8 != (v_scale_new != nullptr)) return PA_ERR_DTYPE;
+  const bool q8 = cache->dtype != PA_KV_BF16;  // 8-bit codes with scales
+  if (q8 != (k_scale_new != nullptr) || q8 != (v_scale_new != nullptr)) return PA_ERR_DTYPE;
   if (!aligned16(k) || !aligned16(v)) return PA_ERR_ALIGN;
   DeviceInfo* dev = nullptr;
   if ((st = device_info(&dev)) != PA_OK) return st;
@@ -201,8 +202,8 @@ pa_status pa_store_kv(const void* k, const void* v, const float* k_scale_new,
   a.slot_mapping = slot_mapping;
   a.k_cache = cache->k_cache;
   a.v_cache = cache->v_cache;
-  a.k_scale = fp8 ? cache->k_scale : nullptr;
-  a.v_scale = fp8 ? cache->v_scale : nullptr;
+  a.k_scale = q8 ? cache->k_scale : nullptr;
+  a.v_scale = q8 ? cache->v_scale : nullptr;
   a.num_tokens = num_tokens;
   a.row_bytes = cache->num_kv_heads * cache->head_dim * elem_bytes(cache);
   a.num_kv_heads = cache->num_kv_heads;
@@ -221,7 +222,7 @@ size_t pa_decode_workspace_size(const pa_kv_cache* cache, int32_t batch, int32_t
   if (device_info(&dev) != PA_OK) return 0;
   const int cap = decode_len_cap(cache, max_blocks_per_seq, max_context_len);
   return pa::plan_decode(batch, num_heads, cache->num_kv_heads, cache->head_dim, cache->block_size,
-                         cache->dtype == PA_KV_FP8_E4M3, cap, dev->num_sms)
+                         static_cast<int>(cache->dtype), cap, dev->num_sms)
       .workspace_bytes;
 }
 
@@ -252,9 +253,10 @@ pa_status decode_common(const void* q, const pa_kv_cache* cache, const int32_t* 
   DeviceInfo* dev = nullptr;
   if ((st = device_info(&dev)) != PA_OK) return st;
   const int cap = decode_len_cap(cache, max_blocks_per_seq, max_context_len);
-  const bool fp8 = cache->dtype == PA_KV_FP8_E4M3;
+  const bool q8 = cache->dtype != PA_KV_BF16;  // 8-bit codes with scales
   const pa::DecodePlan plan = pa::plan_decode(batch, num_heads, cache->num_kv_heads,
-                                              cache->head_dim, cache->block_size, fp8, cap,
+                                              cache->head_dim, cache->block_size,
+                                              static_cast<int>(cache->dtype), cap,
                                               dev->num_sms);
   if (plan.workspace_bytes > 0 &&
       (workspace == nullptr || workspace_bytes < plan.workspace_bytes || !aligned16(workspace)))
@@ -274,8 +276,8 @@ pa_status decode_common(const void* q, const pa_kv_cache* cache, const int32_t* 
     s.v_scale_new = v_scale_new;
     s.k_cache = cache->k_cache;
     s.v_cache = cache->v_cache;
-    s.k_scale = fp8 ? cache->k_scale : nullptr;
-    s.v_scale = fp8 ? cache->v_scale : nullptr;
+    s.k_scale = q8 ? cache->k_scale : nullptr;
+    s.v_scale = q8 ? cache->v_scale : nullptr;
     s.num_tokens = batch;
     s.row_bytes = cache->num_kv_heads * cache->head_dim * elem_bytes(cache);
     s.num_kv_heads = cache->num_kv_heads;
@@ -291,15 +293,15 @@ pa_status decode_common(const void* q, const pa_kv_cache* cache, const int32_t* 
   if (fused_append) {
     a.k_new = k_new;
     a.v_new = v_new;
-    a.k_scale_new = fp8 ? k_scale_new : nullptr;
-    a.v_scale_new = fp8 ? v_scale_new : nullptr;
+    a.k_scale_new = q8 ? k_scale_new : nullptr;
+    a.v_scale_new = q8 ? v_scale_new : nullptr;
     a.k_cache = cache->k_cache;
     a.v_cache = cache->v_cache;
   }
   a.block_tables = block_tables;
   a.context_lens = context_lens;
-  a.k_scale = fp8 ? cache->k_scale : nullptr;
-  a.v_scale = fp8 ? cache->v_scale : nullptr;
+  a.k_scale = q8 ? cache->k_scale : nullptr;
+  a.v_scale = q8 ? cache->v_scale : nullptr;
   a.out = out;
   a.slot_rows = plan.slot_rows;
   if (plan.workspace_bytes > 0) {
@@ -327,7 +329,7 @@ pa_status decode_common(const void* q, const pa_kv_cache* cache, const int32_t* 
   a.persistent_ctas = plan.persistent_ctas;
   a.blocks_per_split = plan.blocks_per_split;
   a.num_splits = plan.num_splits;
-  a.fp8 = fp8;
+  a.kv = static_cast<int>(cache->dtype);
   a.scale_log2 = scale * 1.4426950408889634f;  // log2(e): scores kept in base-2 units
   return pa::launch_decode(a, kmap, vmap, strm) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
@@ -365,8 +367,8 @@ pa_status pa_decode_append(const void* q, const void* k_new, const void* v_new,
   pa_status st = check_cache(cache);
   if (st != PA_OK) return st;
   if (batch > 0 && (k_new == nullptr || v_new == nullptr)) return PA_ERR_NULL;
-  const bool fp8 = cache->dtype == PA_KV_FP8_E4M3;
-  if (fp8 != (k_scale_new != nullptr) || fp8 != (v_scale_new != nullptr)) return PA_ERR_DTYPE;
+  const bool q8 = cache->dtype != PA_KV_BF16;  // 8-bit codes with scales
+  if (q8 != (k_scale_new != nullptr) || q8 != (v_scale_new != nullptr)) return PA_ERR_DTYPE;
   if (batch > 0 && (!aligned16(k_new) || !aligned16(v_new))) return PA_ERR_ALIGN;
   return decode_common(q, cache, block_tables, max_blocks_per_seq, context_lens, max_context_len,
                        batch, num_heads, scale, out, workspace, workspace_bytes, stream, k_new,

@@ -19,17 +19,20 @@
 //   * All G = H/Hkv query heads of a kv head share every K/V tile (GQA).
 //   * Each warp streams its blocks through a private ring of shared-memory
 //     stages filled by TMA (3-D tiled loads of one block of one kv head,
-//     128B-swizzled; FP8 scales by 1-D bulk copies), tracked by mbarriers with
-//     bounded waits. Loads run ahead across segment boundaries, and the block
-//     id of the next load is fetched one step early to hide its latency.
+//     128B-swizzled; 8-bit-code scales by 1-D bulk copies), tracked by
+//     mbarriers with bounded waits. Loads run ahead across segment boundaries;
+//     block ids are read 32 at a time, a window ahead of the loads.
 //   * The two contractions per block, S = Q K^T (heads x tokens over head_dim)
 //     and O^T += V^T P^T (head_dim x heads over tokens), run on the warp-level
 //     tensor-core MMA (m16n8k16, fp32 accumulate). The softmax is online
 //     ("tiny-vllm part 05", pagedAttentionKernel section): a running max and
 //     sum per head, reduced over the 4 lanes that share a head with warp
 //     shuffles, accumulators rescaled when the max grows.
-//   * FP8-E4M3 KV: codes are widened exactly to f16 in registers; the K scale
-//     multiplies the score, the V scale multiplies the probability.
+//   * 8-bit KV (E4M3 or INT8 codes, flag Q8): codes are widened exactly to
+//     f16 in registers; the K scale multiplies the score, the V scale the
+//     probability.
+//   * A sliding window with sinks (WIN) walks only the blocks that hold a
+//     visible key and masks the rest inside them.
 //   * Batches above kMaxPersistentBatch use a grid of (kv head, sequence,
 //     split) CTAs instead, with the same per-block code.
 #include <algorithm>
@@ -45,22 +48,22 @@ namespace {
 constexpr unsigned kFull = 0xffffffffu;
 constexpr int kMaxDevices = 64;
 
-template <int D, int BS, int NW, int ST, bool FP8>
+template <int D, int BS, int NW, int ST, bool Q8>
 struct Cfg {
-  static constexpr int kElem = FP8 ? 1 : 2;
+  static constexpr int kElem = Q8 ? 1 : 2;
   static constexpr int kRowBytes = D * kElem;                  // one (token, kv head) row
   static constexpr int kNSub = kRowBytes / kSwizzleBytes;      // 128-byte-wide subtiles per row
   static constexpr int kSubBytes = BS * kSwizzleBytes;
   static constexpr int kTile = kNSub * kSubBytes;              // K (or V) of one block, one kv head
   static constexpr int kStage = 2 * kTile;
   static constexpr int kTiles = NW * ST * kStage;
-  static constexpr int kScaleBytes = FP8 ? NW * ST * 2 * BS * 4 : 0;
+  static constexpr int kScaleBytes = Q8 ? NW * ST * 2 * BS * 4 : 0;
   static constexpr int kMoStride = D + 4;                      // padded row of the merge buffer
   static constexpr int kMerge = NW * 8 * kMoStride * 4 + NW * 8 * 2 * 4;
-  static constexpr uint32_t kTx = kStage + (FP8 ? 2 * BS * 4 : 0);
+  static constexpr uint32_t kTx = kStage + (Q8 ? 2 * BS * 4 : 0);
   static_assert(kRowBytes % kSwizzleBytes == 0, "row must be a multiple of 128 bytes");
   static_assert(BS % 16 == 0, "block size must be a multiple of 16");
-  static_assert(!FP8 || D == 128, "FP8 path is written for head_dim 128");
+  static_assert(!Q8 || D == 128, "the 8-bit path is written for head_dim 128");
   static_assert(kMerge % 16 == 0, "merge buffer must keep 16-byte alignment");
 };
 
@@ -75,10 +78,10 @@ __device__ __forceinline__ uint32_t swz(uint32_t tile, int row, int chunk) {
 // Q fragments (A operand of S = Q K^T) of kv head `kvh` of sequence b:
 // MMA row r = head r of the group (rows >= G are zero).
 // bf16: k index of step ks = head_dim ks*16 + {2q4, 2q4+1, 2q4+8, 2q4+9}.
-// FP8 (f16 MMA): the head_dim order inside a step is permuted to match how
+// 8-bit codes (f16 MMA): the head_dim order inside a step is permuted to match how
 // the K codes are read (lane quad q4 owns dims [32 q4, 32 q4 + 32)): step ks
 // uses dims 32 q4 + 4 ks + {0,1} (k = 2q4, 2q4+1) and + {2,3} (k = 2q4+8, +9).
-template <int D, bool FP8>
+template <int D, bool Q8>
 __device__ __forceinline__ void load_q(const DecodeArgs& a, int b, int kvh, int lane,
                                        uint32_t (&qa)[D / 16][2]) {
   const int G = a.group, r = lane >> 2, q4 = lane & 3;
@@ -87,7 +90,7 @@ __device__ __forceinline__ void load_q(const DecodeArgs& a, int b, int kvh, int 
 #pragma unroll
   for (int ks = 0; ks < D / 16; ++ks) {
     if (r < G) {
-      if constexpr (!FP8) {
+      if constexpr (!Q8) {
         qa[ks][0] = *reinterpret_cast<const uint32_t*>(qrow + ks * 16 + 2 * q4);
         qa[ks][1] = *reinterpret_cast<const uint32_t*>(qrow + ks * 16 + 8 + 2 * q4);
       } else {
@@ -105,12 +108,12 @@ __device__ __forceinline__ void load_q(const DecodeArgs& a, int b, int kvh, int 
 }
 
 // One physical block (tokens tok0 .. tok0+BS-1, of which those < L count)
-// staged in shared memory at kt (K) / vt (V), FP8 scales at ksc / vsc:
+// staged in shared memory at kt (K) / vt (V), 8-bit-code scales at ksc / vsc:
 // fold it into the warp's online-softmax state (m_run, l_run for head r of
 // lane group r; acc = O^T fragments for heads 2q4, 2q4+1). The whole block is
 // one softmax step: S for its BS tokens (BS/8 n-tiles, independent MMA
 // chains), one max/sum update, then P.V per 16-token group.
-template <int D, int BS, bool FP8, bool HOLE = false>
+template <int D, int BS, int KV, bool HOLE = false>
 __device__ __forceinline__ void attend_block(uint32_t kt, uint32_t vt, const uint8_t* base_ptr,
                                              uint32_t base, const float* ksc, const float* vsc,
                                              int tok0, int L, int hole_lo, int hole_hi,
@@ -119,6 +122,7 @@ __device__ __forceinline__ void attend_block(uint32_t kt, uint32_t vt, const uin
                                              float sl2, int lane) {
   constexpr int NT = BS / 8;  // n-tiles of 8 tokens
   constexpr int NG = BS / 16;  // 16-token groups (k-steps of P.V)
+  constexpr bool Q8 = KV != kKvBf16;
   const int r = lane >> 2, q4 = lane & 3;
   // keys t < L outside the window's hole [hole_lo, hole_hi) take part
   auto valid = [&](int t) { return t < L && (!HOLE || t < hole_lo || t >= hole_hi); };
@@ -127,7 +131,7 @@ __device__ __forceinline__ void attend_block(uint32_t kt, uint32_t vt, const uin
   float sc[NT][4];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
-  if constexpr (!FP8) {
+  if constexpr (!Q8) {
     const int mi = lane >> 3;
 #pragma unroll
     for (int ks = 0; ks < D / 16; ++ks) {
@@ -156,7 +160,7 @@ __device__ __forceinline__ void attend_block(uint32_t kt, uint32_t vt, const uin
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
         uint32_t b0, b1;
-        e4m3x4_to_f16x2x2(w[nt][ks], b0, b1);
+        codes8x4_to_f16x2x2<KV>(w[nt][ks], b0, b1);
         mma_f16(sc[nt], qa[ks][0], 0u, qa[ks][1], 0u, b0, b1);
       }
     }
@@ -165,7 +169,7 @@ __device__ __forceinline__ void attend_block(uint32_t kt, uint32_t vt, const uin
   float x[2 * NT];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
-    if constexpr (!FP8) {
+    if constexpr (!Q8) {
       x[2 * nt] = sc[nt][0] * sl2;
       x[2 * nt + 1] = sc[nt][1] * sl2;
     } else {
@@ -219,7 +223,7 @@ __device__ __forceinline__ void attend_block(uint32_t kt, uint32_t vt, const uin
       mhi = (valid(g0 + 8) ? 0x0000ffffu : 0u) | (valid(g0 + 9) ? 0xffff0000u : 0u);
     }
     const float p0 = pr[4 * hg], p1 = pr[4 * hg + 1], p8 = pr[4 * hg + 2], p9 = pr[4 * hg + 3];
-    if constexpr (!FP8) {
+    if constexpr (!Q8) {
       const uint32_t pb0 = pack_bf16x2(p0, p1);
       const uint32_t pb1 = pack_bf16x2(p8, p9);
       const int mi = lane >> 3;
@@ -263,8 +267,8 @@ __device__ __forceinline__ void attend_block(uint32_t kt, uint32_t vt, const uin
         for (int o = 0; o < 2; ++o) {
           const uint32_t sel = o ? 0x7362u : 0x5140u;
           uint32_t a0, a1, a2, a3;
-          e4m3x4_to_f16x2x2(prmt(w0[w], w1[w], sel), a0, a1);
-          e4m3x4_to_f16x2x2(prmt(w8[w], w9[w], sel), a2, a3);
+          codes8x4_to_f16x2x2<KV>(prmt(w0[w], w1[w], sel), a0, a1);
+          codes8x4_to_f16x2x2<KV>(prmt(w8[w], w9[w], sel), a2, a3);
           if (partial) {
             a0 &= mlo;
             a1 &= mlo;
@@ -279,7 +283,7 @@ __device__ __forceinline__ void attend_block(uint32_t kt, uint32_t vt, const uin
 }
 
 // Write a warp's (max, sum, O) for its 8 head rows into the merge buffer.
-template <int D, int NW, bool FP8>
+template <int D, int NW, bool Q8>
 __device__ __forceinline__ void store_warp_state(float* mo, int warp, int lane, float m_run,
                                                  float l_run, const float (&acc)[D / 16][4]) {
   constexpr int S = D + 4;
@@ -295,7 +299,7 @@ __device__ __forceinline__ void store_warp_state(float* mo, int warp, int lane, 
 #pragma unroll
   for (int mt = 0; mt < D / 16; ++mt) {
     int d0, d1;
-    if constexpr (!FP8) {
+    if constexpr (!Q8) {
       d0 = mt * 16 + r;
       d1 = d0 + 8;
     } else {
@@ -435,7 +439,7 @@ __device__ __forceinline__ void piece_next(Piece& p, const int* prefix, int B, i
 // segment is entirely this warp's, else an fp32 partial (O unnormalised,
 // (max, sum) per head) in `slot`. Lane (r, q4) holds O^T for heads 2q4, 2q4+1
 // and the running max/sum of head r.
-template <int D, bool FP8>
+template <int D, bool Q8>
 __device__ __forceinline__ void write_warp_result(const DecodeArgs& a, int b, int kvh,
                                                   bool final_out, long long slot, int lane,
                                                   float m_run, float l_run,
@@ -453,7 +457,7 @@ __device__ __forceinline__ void write_warp_result(const DecodeArgs& a, int b, in
 #pragma unroll
     for (int mt = 0; mt < D / 16; ++mt) {
       int d0, d1;
-      if constexpr (!FP8) { d0 = mt * 16 + r; d1 = d0 + 8; }
+      if constexpr (!Q8) { d0 = mt * 16 + r; d1 = d0 + 8; }
       else { d0 = 16 * r + 4 * (mt >> 1) + 2 * (mt & 1); d1 = d0 + 1; }
       if (h0 < G) {
         o[h0 * D + d0] = __float2bfloat16_rn(acc[mt][0] * inv0);
@@ -470,7 +474,7 @@ __device__ __forceinline__ void write_warp_result(const DecodeArgs& a, int b, in
 #pragma unroll
   for (int mt = 0; mt < D / 16; ++mt) {
     int d0, d1;
-    if constexpr (!FP8) { d0 = mt * 16 + r; d1 = d0 + 8; }
+    if constexpr (!Q8) { d0 = mt * 16 + r; d1 = d0 + 8; }
     else { d0 = 16 * r + 4 * (mt >> 1) + 2 * (mt & 1); d1 = d0 + 1; }
     if (h0 < G) {
       po[h0 * D + d0] = acc[mt][0];
@@ -648,9 +652,9 @@ __device__ __forceinline__ void merge_segment(const DecodeArgs& a, const SegPart
   else merge_segment_g<D, 8>(a, sp, b, kvh, lane);
 }
 
-template <int D, int BS, int NW, int ST, bool FP8>
+template <int D, int BS, int NW, int ST, bool Q8>
 struct PCfg {
-  using C = Cfg<D, BS, NW, ST, FP8>;
+  using C = Cfg<D, BS, NW, ST, Q8>;
   static constexpr int kScaleOff = C::kTiles;
   static constexpr int kPrefixOff = kScaleOff + C::kScaleBytes;
   static int smem_bytes(int batch) { return 1024 + kPrefixOff + (batch + 1) * 4; }
@@ -658,13 +662,13 @@ struct PCfg {
 
 // Fused append (pa_decode_append): the new token of segment (b, kvh) is row t
 // of its last block. The warp that attends to that block copies the row from
-// k_new / v_new (row `bk` = b * Hkv + kvh) into the staged tile (and the FP8
+// k_new / v_new (row `bk` = b * Hkv + kvh) into the staged tile (and the 8-bit
 // scales into the staged scales) and into the cache slot. Kept out of line:
 // it runs once per segment and must not add registers to the block loop.
-template <int D, int BS, bool FP8>
+template <int D, int BS, bool Q8>
 __device__ __noinline__ void append_row(uint8_t* tile, float* stage_scales, const int32_t* bt_entry,
                                         int bk, int t, const DecodeArgs a, int lane) {
-  constexpr int kRowBytes = D * (FP8 ? 1 : 2);
+  constexpr int kRowBytes = D * (Q8 ? 1 : 2);
   constexpr int kChunks = kRowBytes / 16;
   constexpr int kTile = (kRowBytes / kSwizzleBytes) * BS * kSwizzleBytes;
   const int phys = *bt_entry;
@@ -682,7 +686,7 @@ __device__ __noinline__ void append_row(uint8_t* tile, float* stage_scales, cons
                                 ((static_cast<long long>(phys) * BS + t) * Hkv + kvh) * kRowBytes +
                                 16 * c) = val;
   }
-  if constexpr (FP8) {
+  if constexpr (Q8) {
     if (lane == 0) {
       const float kn = a.k_scale_new[bk], vn = a.v_scale_new[bk];
       stage_scales[t] = kn;
@@ -699,12 +703,13 @@ __device__ __noinline__ void append_row(uint8_t* tile, float* stage_scales, cons
   __syncwarp();
 }
 
-template <int D, int BS, int NW, int ST, bool FP8, bool WIN>
+template <int D, int BS, int NW, int ST, int KV, bool WIN>
 __global__ void __launch_bounds__(NW * 32, 3)
     decode_persistent_kernel(const __grid_constant__ CUtensorMap kmap,
                              const __grid_constant__ CUtensorMap vmap, const DecodeArgs a) {
-  using C = Cfg<D, BS, NW, ST, FP8>;
-  using PC = PCfg<D, BS, NW, ST, FP8>;
+  constexpr bool Q8 = KV != kKvBf16;
+  using C = Cfg<D, BS, NW, ST, Q8>;
+  using PC = PCfg<D, BS, NW, ST, Q8>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bars[NW * ST];
   __shared__ int warp_sums[NW];
@@ -838,7 +843,7 @@ __global__ void __launch_bounds__(NW * 32, 3)
         tma_load_3d(kt + C::kTile + j * C::kSubBytes, &vmap, bar,
                     j * (kSwizzleBytes / C::kElem), kvh, phys * BS, l2_policy);
       }
-      if constexpr (FP8) {
+      if constexpr (Q8) {
         const long long off = (static_cast<long long>(phys) * Hkv + kvh) * BS;
         const uint32_t sc = scale_base + ((warp * ST + s) * 2) * BS * 4;
         bulk_load(sc, a.k_scale + off, BS * 4, bar, l2_policy);
@@ -864,7 +869,7 @@ __global__ void __launch_bounds__(NW * 32, 3)
   bool ok = true;
   while (ok && cp.valid) {
     uint32_t qa[D / 16][2];
-    load_q<D, FP8>(a, cp.b, cp.kvh, lane, qa);
+    load_q<D, Q8>(a, cp.b, cp.kvh, lane, qa);
     const int L = min(max(a.context_lens[cp.b], 0), a.len_cap);
     const SeqWindow sw = seq_window<BS>(L, WIN ? a.window : 0, a.sinks);
     float acc[D / 16][4];
@@ -883,11 +888,11 @@ __global__ void __launch_bounds__(NW * 32, 3)
       const uint32_t kt = stage0 + s * C::kStage;
       const float* ksc = scale_ptr + ((warp * ST + s) * 2) * BS;
       if (a.k_new != nullptr && vb == cp.nblk - 1)
-        append_row<D, BS, FP8>(base_ptr + (kt - base),
+        append_row<D, BS, Q8>(base_ptr + (kt - base),
                                const_cast<float*>(scale_ptr) + ((warp * ST + s) * 2) * BS,
                                a.block_tables + static_cast<long long>(cp.b) * a.max_blocks + blk,
                                cp.b * Hkv + cp.kvh, (L - 1) - blk * BS, a, lane);
-      attend_block<D, BS, FP8, WIN>(kt, kt + C::kTile, base_ptr, base, ksc, ksc + BS, blk * BS, L,
+      attend_block<D, BS, KV, WIN>(kt, kt + C::kTile, base_ptr, base, ksc, ksc + BS, blk * BS, L,
                                     sw.hole_lo, sw.hole_hi, qa, acc, m_run, l_run, sl2, lane);
       ++consumed;
       __syncwarp();
@@ -895,7 +900,7 @@ __global__ void __launch_bounds__(NW * 32, 3)
     }
     if (!ok) break;
     const bool whole = cp.lo == 0 && cp.hi == cp.nblk;
-    write_warp_result<D, FP8>(a, cp.b, cp.kvh, whole, 2 * gw + (cp.lo == 0 ? 1 : 0), lane, m_run,
+    write_warp_result<D, Q8>(a, cp.b, cp.kvh, whole, 2 * gw + (cp.lo == 0 ? 1 : 0), lane, m_run,
                               l_run, acc);
     if (!whole) {
       // publish the partial, count the arrival; the last warp merges the segment
@@ -922,11 +927,12 @@ __global__ void __launch_bounds__(NW * 32, 3)
 // ============================================================ grid-split path
 // Grid (Hkv, B, S): CTA = (kv head, sequence, split of blocks_per_split
 // blocks). Used for batches too large for the persistent kernel's prefix.
-template <int D, int BS, int NW, int ST, bool FP8>
+template <int D, int BS, int NW, int ST, int KV>
 __global__ void __launch_bounds__(NW * 32)
     decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
                         const __grid_constant__ CUtensorMap vmap, const DecodeArgs a) {
-  using C = Cfg<D, BS, NW, ST, FP8>;
+  constexpr bool Q8 = KV != kKvBf16;
+  using C = Cfg<D, BS, NW, ST, Q8>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bars[NW * ST];
 
@@ -982,7 +988,7 @@ __global__ void __launch_bounds__(NW * 32)
         tma_load_3d(kt + C::kTile + j * C::kSubBytes, &vmap, bar,
                     j * (kSwizzleBytes / C::kElem), kvh, phys * BS);
       }
-      if constexpr (FP8) {
+      if constexpr (Q8) {
         const long long off = (static_cast<long long>(phys) * a.num_kv_heads + kvh) * BS;
         const uint32_t sc = scale_base + ((warp * ST + s) * 2) * BS * 4;
         bulk_load(sc, a.k_scale + off, BS * 4, bar);
@@ -995,7 +1001,7 @@ __global__ void __launch_bounds__(NW * 32)
   for (int i = 0; i < n_pre; ++i) issue(i);
 
   uint32_t qa[D / 16][2];
-  load_q<D, FP8>(a, b, kvh, lane, qa);
+  load_q<D, Q8>(a, b, kvh, lane, qa);
   float acc[D / 16][4];
 #pragma unroll
   for (int mt = 0; mt < D / 16; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
@@ -1013,7 +1019,7 @@ __global__ void __launch_bounds__(NW * 32)
     consumed = i + 1;
     const uint32_t kt = stage0 + s * C::kStage;
     const float* ksc = scale_ptr + ((warp * ST + s) * 2) * BS;
-    attend_block<D, BS, FP8>(kt, kt + C::kTile, base_ptr, base, ksc, ksc + BS,
+    attend_block<D, BS, KV>(kt, kt + C::kTile, base_ptr, base, ksc, ksc + BS,
                              (blk0 + warp + i * NW) * BS, L, 0, 0, qa, acc, m_run, l_run,
                              a.scale_log2, lane);
     __syncwarp();
@@ -1024,7 +1030,7 @@ __global__ void __launch_bounds__(NW * 32)
     for (int i = consumed; i < min(n_my, consumed + ST); ++i)
       (void)mbar_wait(bar0 + 8 * (i % ST), (i / ST) & 1);
   }
-  store_warp_state<D, NW, FP8>(merge_buf, warp, lane, m_run, l_run, acc);
+  store_warp_state<D, NW, Q8>(merge_buf, warp, lane, m_run, l_run, acc);
   const bool any_fail = __syncthreads_or(!ok);
   if (any_fail) return;
   // partial slot of (b, kvh, split): the merge kernel below reads these
@@ -1091,11 +1097,12 @@ constexpr int stages_for(int stage_bytes) {
                                                      : kStageBudget / (kWarps * stage_bytes);
 }
 
-template <int D, int BS, bool FP8>
+template <int D, int BS, int KV>
 struct Inst {
-  static constexpr int kStages = stages_for(Cfg<D, BS, kWarps, 2, FP8>::kStage);
-  using C = Cfg<D, BS, kWarps, kStages, FP8>;
-  using PC = PCfg<D, BS, kWarps, kStages, FP8>;
+  static constexpr bool Q8 = KV != kKvBf16;
+  static constexpr int kStages = stages_for(Cfg<D, BS, kWarps, 2, Q8>::kStage);
+  using C = Cfg<D, BS, kWarps, kStages, Q8>;
+  using PC = PCfg<D, BS, kWarps, kStages, Q8>;
   static constexpr int kSplitSmem = 1024 + C::kTiles + C::kScaleBytes + C::kMerge;
   static_assert(kSplitSmem <= 227 * 1024, "shared memory over the per-CTA limit");
   static_assert(PC::kPrefixOff + 1024 + (kMaxPersistentBatch + 1) * 4 <= 227 * 1024,
@@ -1111,8 +1118,8 @@ struct Inst {
     if (cached[dev] > 0) return cached[dev];
     // both variants (with and without a sliding window) get the attribute;
     // the grid is sized by the one with fewer resident CTAs
-    auto* k0 = decode_persistent_kernel<D, BS, kWarps, kStages, FP8, false>;
-    auto* k1 = decode_persistent_kernel<D, BS, kWarps, kStages, FP8, true>;
+    auto* k0 = decode_persistent_kernel<D, BS, kWarps, kStages, KV, false>;
+    auto* k1 = decode_persistent_kernel<D, BS, kWarps, kStages, KV, true>;
     const int smem = PC::smem_bytes(kMaxPersistentBatch);
     int n0 = 0, n1 = 0;
     if (cudaFuncSetAttribute(k0, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
@@ -1131,8 +1138,8 @@ struct Inst {
     cudaError_t e;
     const long long rows = static_cast<long long>(a.batch) * a.num_heads;
     if (a.persistent_ctas > 0) {
-      auto* k = a.window > 0 ? decode_persistent_kernel<D, BS, kWarps, kStages, FP8, true>
-                             : decode_persistent_kernel<D, BS, kWarps, kStages, FP8, false>;
+      auto* k = a.window > 0 ? decode_persistent_kernel<D, BS, kWarps, kStages, KV, true>
+                             : decode_persistent_kernel<D, BS, kWarps, kStages, KV, false>;
       (void)ctas_per_sm();  // makes sure the shared-memory attribute is set on this device
       // programmatic dependent launch: the prologue may overlap the kernel
       // before this one on the stream (the kernel waits before reading K/V)
@@ -1148,7 +1155,7 @@ struct Inst {
       cfg.numAttrs = 1;
       return cudaLaunchKernelEx(&cfg, k, kmap, vmap, a);
     }
-    auto* k = decode_split_kernel<D, BS, kWarps, kStages, FP8>;
+    auto* k = decode_split_kernel<D, BS, kWarps, kStages, KV>;
     static bool attr_set[kMaxDevices] = {};
     int dev = 0;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
@@ -1176,24 +1183,29 @@ int split_tokens_target() {
 }
 
 template <typename F>
-auto dispatch(int head_dim, int block_size, bool fp8, F&& f) -> decltype(f(Inst<128, 16, false>{})) {
-  if (fp8) {
-    if (head_dim == 128 && block_size == 16) return f(Inst<128, 16, true>{});
-    return f(Inst<128, 32, true>{});
+auto dispatch(int head_dim, int block_size, int kv, F&& f)
+    -> decltype(f(Inst<128, 16, kKvBf16>{})) {
+  if (kv == kKvE4m3) {
+    if (block_size == 16) return f(Inst<128, 16, kKvE4m3>{});
+    return f(Inst<128, 32, kKvE4m3>{});
   }
-  if (head_dim == 128 && block_size == 16) return f(Inst<128, 16, false>{});
-  if (head_dim == 128 && block_size == 32) return f(Inst<128, 32, false>{});
-  if (head_dim == 64 && block_size == 16) return f(Inst<64, 16, false>{});
-  return f(Inst<64, 32, false>{});
+  if (kv == kKvInt8) {
+    if (block_size == 16) return f(Inst<128, 16, kKvInt8>{});
+    return f(Inst<128, 32, kKvInt8>{});
+  }
+  if (head_dim == 128 && block_size == 16) return f(Inst<128, 16, kKvBf16>{});
+  if (head_dim == 128 && block_size == 32) return f(Inst<128, 32, kKvBf16>{});
+  if (head_dim == 64 && block_size == 16) return f(Inst<64, 16, kKvBf16>{});
+  return f(Inst<64, 32, kKvBf16>{});
 }
 
 }  // namespace
 
 DecodePlan plan_decode(int batch, int num_heads, int num_kv_heads, int head_dim, int block_size,
-                       bool fp8, int len_cap, int num_sms) {
+                       int kv, int len_cap, int num_sms) {
   DecodePlan p{};
   if (batch <= kMaxPersistentBatch) {
-    const int per_sm = dispatch(head_dim, block_size, fp8,
+    const int per_sm = dispatch(head_dim, block_size, kv,
                                 [&](auto inst) { return decltype(inst)::ctas_per_sm(); });
     p.persistent_ctas = per_sm * num_sms;
     p.blocks_per_split = 0;
@@ -1234,10 +1246,10 @@ DecodePlan plan_decode(int batch, int num_heads, int num_kv_heads, int head_dim,
 
 cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
                           cudaStream_t stream) {
-  if (a.fp8 && a.head_dim != 128) return cudaErrorInvalidValue;
+  if (a.kv != kKvBf16 && a.head_dim != 128) return cudaErrorInvalidValue;
   if ((a.head_dim != 64 && a.head_dim != 128) || (a.block_size != 16 && a.block_size != 32))
     return cudaErrorInvalidValue;
-  return dispatch(a.head_dim, a.block_size, a.fp8,
+  return dispatch(a.head_dim, a.block_size, a.kv,
                   [&](auto inst) { return decltype(inst)::launch(a, kmap, vmap, stream); });
 }
 

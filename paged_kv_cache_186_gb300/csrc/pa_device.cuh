@@ -215,6 +215,25 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   return r;
 }
 
+// Four signed INT8 codes (one 32-bit word) -> two f16x2, exactly (|code| <=
+// 128 is representable): each byte b, with its sign bit flipped, becomes the
+// low mantissa byte of f16 1024 (0x6400), giving 1024 + b + 128; subtracting
+// 1152 (0x6480) leaves b. `lo` from bytes 0-1, `hi` from bytes 2-3.
+__device__ __forceinline__ void s8x4_to_f16x2x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  const uint32_t u = w ^ 0x80808080u;
+  lo = prmt(u, 0x64646464u, 0x4140u);
+  hi = prmt(u, 0x64646464u, 0x4342u);
+  asm("sub.rn.f16x2 %0, %0, %1;" : "+r"(lo) : "r"(0x64806480u));
+  asm("sub.rn.f16x2 %0, %0, %1;" : "+r"(hi) : "r"(0x64806480u));
+}
+
+// Four 8-bit codes of kind KV (1 = E4M3, 2 = INT8) -> two f16x2.
+template <int KV>
+__device__ __forceinline__ void codes8x4_to_f16x2x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  if constexpr (KV == 2) s8x4_to_f16x2x2(w, lo, hi);
+  else e4m3x4_to_f16x2x2(w, lo, hi);
+}
+
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));

@@ -37,13 +37,17 @@ cudaError_t launch_store_new_tokens(const StoreArgs& a, const int32_t* block_tab
 
 // Largest batch the persistent decode kernel handles (its per-sequence block
 // prefix sums live in shared memory); larger batches use the grid-split kernel.
+// KV element kinds (the pa_kv_dtype values): bf16, or 8-bit codes with
+// per-(slot, head) scales in E4M3 or INT8.
+constexpr int kKvBf16 = 0, kKvE4m3 = 1, kKvInt8 = 2;
+
 constexpr int kMaxPersistentBatch = 2048;
 
 struct DecodeArgs {
   const void* q;              // (B, H, D) bf16
   const int32_t* block_tables;
   const int32_t* context_lens;
-  const float* k_scale;       // FP8: (NB, Hkv, bs)
+  const float* k_scale;       // 8-bit caches: (NB, Hkv, bs)
   const float* v_scale;
   void* out;                  // (B, H, D) bf16
   float* part_o;              // partial slots: (slots, 8, D) fp32
@@ -57,7 +61,7 @@ struct DecodeArgs {
   // context_lens[b]-1, is written to the cache by the warp that attends to it
   const void* k_new;          // (B, Hkv, D) cache dtype, or NULL
   const void* v_new;
-  const float* k_scale_new;   // FP8: (B, Hkv)
+  const float* k_scale_new;   // 8-bit caches: (B, Hkv)
   const float* v_scale_new;
   void* k_cache;              // cache base pointers (written when appending)
   void* v_cache;
@@ -66,7 +70,7 @@ struct DecodeArgs {
   int window, sinks;          // sliding window (> 0) with leading sink keys; 0 = all keys
   int persistent_ctas;        // > 0: persistent kernel with this many CTAs
   int blocks_per_split, num_splits;  // grid-split path
-  bool fp8;
+  int kv;                     // kKvBf16, kKvE4m3 or kKvInt8
   float scale_log2;
 };
 
@@ -82,7 +86,7 @@ struct DecodePlan {
 };
 
 DecodePlan plan_decode(int batch, int num_heads, int num_kv_heads, int head_dim, int block_size,
-                       bool fp8, int len_cap, int num_sms);
+                       int kv, int len_cap, int num_sms);
 
 cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
                           cudaStream_t stream);

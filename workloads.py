@@ -48,6 +48,13 @@ WORKLOADS = {
                                        num_kv_heads=8, head_dim=128, block_size=32,
                                        lens=("lognormal", 1024.0, 1.0, 1, 16384), pool_factor=1.1,
                                        scale=1.0 / math.sqrt(128), kv_dtype="fp8"),
+    # The same continuous batch with an INT8 KV cache (symmetric codes, one
+    # fp32 scale per (token, head)): the glossary's other KV quantisation.
+    "llama3_70b_int8_decode_b256": dict(kind="decode", seed=3, batch=256, num_heads=64,
+                                        num_kv_heads=8, head_dim=128, block_size=32,
+                                        lens=("lognormal", 1024.0, 1.0, 1, 16384),
+                                        pool_factor=1.1, scale=1.0 / math.sqrt(128),
+                                        kv_dtype="int8"),
     # Varlen prefix-cached prefill: 8 sequences, 32/8 heads, D=128, bs=16,
     # cached_len uniform in [0, 2048], q_len uniform in [128, 1024].
     "varlen_prefill_b8": dict(kind="prefill", seed=4, batch=8, num_heads=32, num_kv_heads=8,
