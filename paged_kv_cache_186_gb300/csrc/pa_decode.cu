@@ -1108,29 +1108,39 @@ struct Inst {
   static_assert(PC::kPrefixOff + 1024 + (kMaxPersistentBatch + 1) * 4 <= 227 * 1024,
                 "shared memory over the per-CTA limit");
 
-  // Per device, once: allow the largest shared-memory size any batch needs
-  // and record how many CTAs of it fit on an SM (the persistent grid is that
-  // times the SM count, the same for every call on the device).
-  static int ctas_per_sm() {
-    static int cached[kMaxDevices] = {};
+  // Shared memory grows with the batch (its block prefix sums): batches are
+  // bucketed by 256 sequences. Per device and bucket, once: allow the
+  // largest size any batch needs and record how many CTAs fit on an SM (the
+  // persistent grid is that times the SM count, the same for every call with
+  // a batch in the bucket).
+  static constexpr int kBucket = 256;
+  static constexpr int kBuckets = kMaxPersistentBatch / kBucket;
+  static int bucket_batch(int batch) {
+    return std::max(1, (batch + kBucket - 1) / kBucket) * kBucket;
+  }
+  static int ctas_per_sm(int batch) {
+    static int cached[kMaxDevices][kBuckets] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 1;
-    if (cached[dev] > 0) return cached[dev];
+    const int bb = bucket_batch(std::min(std::max(batch, 1), kMaxPersistentBatch));
+    int& slot = cached[dev][bb / kBucket - 1];
+    if (slot > 0) return slot;
     // both variants (with and without a sliding window) get the attribute;
     // the grid is sized by the one with fewer resident CTAs
     auto* k0 = decode_persistent_kernel<D, BS, kWarps, kStages, KV, false>;
     auto* k1 = decode_persistent_kernel<D, BS, kWarps, kStages, KV, true>;
-    const int smem = PC::smem_bytes(kMaxPersistentBatch);
+    const int smem_max = PC::smem_bytes(kMaxPersistentBatch);
+    const int smem = PC::smem_bytes(bb);
     int n0 = 0, n1 = 0;
-    if (cudaFuncSetAttribute(k0, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+    if (cudaFuncSetAttribute(k0, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max) !=
             cudaSuccess ||
-        cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+        cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max) !=
             cudaSuccess ||
         cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n0, k0, kWarps * 32, smem) != cudaSuccess ||
         cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n1, k1, kWarps * 32, smem) != cudaSuccess)
       return 1;
-    cached[dev] = std::max(1, std::min(n0, n1));
-    return cached[dev];
+    slot = std::max(1, std::min(n0, n1));
+    return slot;
   }
 
   static cudaError_t launch(const DecodeArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
@@ -1140,13 +1150,13 @@ struct Inst {
     if (a.persistent_ctas > 0) {
       auto* k = a.window > 0 ? decode_persistent_kernel<D, BS, kWarps, kStages, KV, true>
                              : decode_persistent_kernel<D, BS, kWarps, kStages, KV, false>;
-      (void)ctas_per_sm();  // makes sure the shared-memory attribute is set on this device
+      (void)ctas_per_sm(a.batch);  // makes sure the shared-memory attribute is set
       // programmatic dependent launch: the prologue may overlap the kernel
       // before this one on the stream (the kernel waits before reading K/V)
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3(a.persistent_ctas);
       cfg.blockDim = dim3(kWarps * 32);
-      cfg.dynamicSmemBytes = PC::smem_bytes(a.batch);
+      cfg.dynamicSmemBytes = PC::smem_bytes(bucket_batch(a.batch));  // the size the grid assumed
       cfg.stream = stream;
       cudaLaunchAttribute attr[1];
       attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -1206,7 +1216,7 @@ DecodePlan plan_decode(int batch, int num_heads, int num_kv_heads, int head_dim,
   DecodePlan p{};
   if (batch <= kMaxPersistentBatch) {
     const int per_sm = dispatch(head_dim, block_size, kv,
-                                [&](auto inst) { return decltype(inst)::ctas_per_sm(); });
+                                [&](auto inst) { return decltype(inst)::ctas_per_sm(batch); });
     p.persistent_ctas = per_sm * num_sms;
     p.blocks_per_split = 0;
     p.num_splits = 0;
