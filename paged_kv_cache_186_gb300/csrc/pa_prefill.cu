@@ -240,34 +240,46 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ MMA issue
     constexpr uint32_t kIdescQK = tc::idesc_bf16_f32(kBM, kBN, false, false);
     constexpr uint32_t kIdescPV = tc::idesc_bf16_f32(kBM, kD, false, true);
-    bool ok = warp_wait(bar(BAR_Q), 0, &abort_flag, a.err);
+    // Order per key tile n: P.V of tile 0, then S of tile 0 for key tile n+1,
+    // then the same for tile 1. Each tile's next S starts as soon as its own
+    // P.V is done, so one tile's softmax runs while the tensor pipe works on
+    // the other tile (S_i and P_i share TMEM columns: S_i(n+1) waits for
+    // P_i V(n) to finish).
+    auto issue_s = [&](int i, int ks) {
+      tc::fence_after_sync();
+      if (lane == 0) {
+#pragma unroll
+        for (int kk = 0; kk < kD / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * kSub + (kk & 3) * 32;
+          tc::mma_ss(tS(i), tc::smem_desc_sw128(q_s(i) + off, 16, 1024),
+                     tc::smem_desc_sw128(k_s(ks) + off, 16, 1024), kIdescQK, kk > 0 ? 1u : 0u);
+        }
+        tc::commit(bar(BAR_S + i));
+      }
+      __syncwarp();
+    };
+    auto issue_pv = [&](int i, int vs, int n) {
+      tc::fence_after_sync();
+      if (lane == 0) {
+#pragma unroll
+        for (int kk = 0; kk < kBN / 16; ++kk)
+          tc::mma_ts(tO(i), tS(i) + kk * 8, tc::smem_desc_sw128(v_s(vs) + kk * 16 * 128, kSub, 1024),
+                     kIdescPV, (n > 0 || kk > 0) ? 1u : 0u);
+        tc::commit(bar(BAR_O + i));
+      }
+      __syncwarp();
+    };
+    bool ok = warp_wait(bar(BAR_Q), 0, &abort_flag, a.err) &&
+              warp_wait(bar(BAR_KF + 0), 0, &abort_flag, a.err);
+    if (ok) {
+      for (int i = 0; i < 2; ++i)
+        if (Tq[i] > 0) issue_s(i, 0);
+      if (lane == 0) tc::commit(bar(BAR_KE + 0));
+      __syncwarp();
+    }
     for (int n = 0; ok && n < T; ++n) {
       const int s = n % kStages;
-      const uint32_t par = (n / kStages) & 1;
-      if (!warp_wait(bar(BAR_KF + s), par, &abort_flag, a.err)) break;
-      for (int i = 0; i < 2; ++i) {
-        if (n >= Tq[i]) continue;
-        // S_i / P_i columns are free once O_i += P_i V of the previous tile is done
-        if (n > 0 && !warp_wait(bar(BAR_O + i), (n - 1) & 1, &abort_flag, a.err)) {
-          ok = false;
-          break;
-        }
-        tc::fence_after_sync();
-        if (lane == 0) {
-#pragma unroll
-          for (int kk = 0; kk < kD / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * kSub + (kk & 3) * 32;
-            tc::mma_ss(tS(i), tc::smem_desc_sw128(q_s(i) + off, 16, 1024),
-                       tc::smem_desc_sw128(k_s(s) + off, 16, 1024), kIdescQK, kk > 0 ? 1u : 0u);
-          }
-          tc::commit(bar(BAR_S + i));
-        }
-        __syncwarp();
-      }
-      if (!ok) break;
-      if (lane == 0) tc::commit(bar(BAR_KE + s));
-      __syncwarp();
-      if (!warp_wait(bar(BAR_VF + s), par, &abort_flag, a.err)) break;
+      if (!warp_wait(bar(BAR_VF + s), (n / kStages) & 1, &abort_flag, a.err)) break;
       // rows of the last, partly filled physical block past kv_len hold
       // whatever the pool had there: zero them so that P = 0 times V stays 0
       const int r0 = kv_len - n * kBN;
@@ -282,24 +294,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async_smem();
         __syncwarp();
       }
+      const bool more = n + 1 < T;  // tile 1 (the later one) needs key tile n+1
+      const int s1 = (n + 1) % kStages;
+      if (more && !warp_wait(bar(BAR_KF + s1), ((n + 1) / kStages) & 1, &abort_flag, a.err))
+        break;
       for (int i = 0; i < 2; ++i) {
         if (n >= Tq[i]) continue;
         if (!warp_wait(bar(BAR_P + i), n & 1, &abort_flag, a.err)) {
           ok = false;
           break;
         }
-        tc::fence_after_sync();
-        if (lane == 0) {
-#pragma unroll
-          for (int kk = 0; kk < kBN / 16; ++kk)
-            tc::mma_ts(tO(i), tS(i) + kk * 8, tc::smem_desc_sw128(v_s(s) + kk * 16 * 128, kSub, 1024),
-                       kIdescPV, (n > 0 || kk > 0) ? 1u : 0u);
-          tc::commit(bar(BAR_O + i));
+        issue_pv(i, s, n);
+        if (n + 1 < Tq[i]) {
+          // S_i / P_i columns are free once this P_i V is done
+          if (!warp_wait(bar(BAR_O + i), n & 1, &abort_flag, a.err)) {
+            ok = false;
+            break;
+          }
+          issue_s(i, s1);
         }
-        __syncwarp();
       }
       if (!ok) break;
-      if (lane == 0) tc::commit(bar(BAR_VE + s));
+      if (lane == 0) {
+        tc::commit(bar(BAR_VE + s));
+        if (more) tc::commit(bar(BAR_KE + s1));
+      }
       __syncwarp();
     }
     if (abort_flag) {  // make sure no MMA is still running before TMEM is freed
