@@ -28,6 +28,12 @@
  *     passed in as `workspace` (pa_decode_noalloc uses a static buffer).
  *   - All calls are asynchronous on `stream` (a cudaStream_t passed as void*;
  *     NULL = the legacy default stream) and never synchronise the host.
+ *     Decode launches may start while the previous launch of this library on
+ *     the stream is finishing (programmatic dependent launch): they read
+ *     context_lens and block_tables before waiting for it, and everything
+ *     else after. No kernel of this library writes those two arrays; a
+ *     caller's own kernel that writes them and lets its dependents start
+ *     early must not directly precede a decode call.
  *   - Argument errors are returned before anything is launched. A launch
  *     failure returns PA_ERR_CUDA. Out-of-range indices found on the device
  *     (a slot beyond the pool, a wait that timed out) never fault: the access

@@ -730,10 +730,13 @@ __global__ void __launch_bounds__(NW * 32, 3)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int B = a.batch, Hkv = a.num_kv_heads;
-  // Launched as a programmatic dependent: everything this kernel reads (the
-  // lengths, block table, q, the cache) may be written by the kernel before
-  // it on the stream, so wait for it before the first read.
-  grid_dependency_wait();
+  // Launched as a programmatic dependent, and lets the next launch (the next
+  // decode step) start early: the prologue below (prefix sums, the split, the
+  // first block-id windows) reads only the lengths and the block tables,
+  // which no kernel of this library writes, and so overlaps the tail of the
+  // previous grid. Everything else (the cache, q, the new rows, the output
+  // and the workspace) is touched only after grid_dependency_wait().
+  grid_launch_dependents();
 
   // ---- blocks per sequence and their exclusive prefix sum (whole CTA)
   int carry = 0;
@@ -762,30 +765,20 @@ __global__ void __launch_bounds__(NW * 32, 3)
   }
   if (threadIdx.x == 0) prefix[B] = carry;
   __syncthreads();
-  if (blockIdx.x == 0) {
-    // sequences without keys: zero output rows (no warp owns any of their blocks)
-    for (int i = threadIdx.x; i < B * a.num_heads * (D / 8); i += NW * 32) {
-      const int row = i / (D / 8), b = row / a.num_heads;
-      if (prefix[b + 1] == prefix[b])
-        reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) +
-                                 static_cast<long long>(row) * D)[i % (D / 8)] = make_uint4(0, 0, 0, 0);
-    }
-  }
 
   // ---- this warp's range; from here on warps are independent
   const long long N = static_cast<long long>(prefix[B]) * Hkv;
   const long long W = active_warps(N, gridDim.x, static_cast<long long>(gridDim.x) * NW);
   const long long gw = static_cast<long long>(blockIdx.x) * NW + warp;
-  if (gw >= W) return;
-  const long long r0 = gw * N / W, r1 = (gw + 1) * N / W;
-  if (r0 >= r1) return;
+  const long long r0 = gw < W ? gw * N / W : 0, r1 = gw < W ? (gw + 1) * N / W : 0;
+  const bool active = r0 < r1;  // warps past W (or with an empty range) only wait
 
   const uint32_t bar0 = smem_addr(&bars[warp * ST]);
   const uint32_t stage0 = base + warp * ST * C::kStage;
   // K/V are read once per call: keep them from evicting the block tables,
   // lengths, q and split partials that later reads want from L2
   const uint64_t l2_policy = l2_evict_first_policy();
-  if (lane == 0) {
+  if (active && lane == 0) {
     for (int s = 0; s < ST; ++s) mbar_init(bar0 + 8 * s, 1);
     fence_barrier_init();
     fence_proxy_async_smem();
@@ -821,6 +814,20 @@ __global__ void __launch_bounds__(NW * 32, 3)
   int cur_kvh, cur_phys, nxt_kvh, nxt_phys;
   load_window(0, cur_kvh, cur_phys);
   load_window(32, nxt_kvh, nxt_phys);
+
+  // ---- from here on: memory the previous launch may write
+  grid_dependency_wait();
+  if (blockIdx.x == 0) {
+    // sequences without keys: zero output rows (no warp owns any of their blocks)
+    for (int i = threadIdx.x; i < B * a.num_heads * (D / 8); i += NW * 32) {
+      const int row = i / (D / 8), b = row / a.num_heads;
+      if (prefix[b + 1] == prefix[b])
+        reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) +
+                                 static_cast<long long>(row) * D)[i % (D / 8)] = make_uint4(0, 0, 0, 0);
+    }
+  }
+  if (!active) return;
+
   long long win_base = 0;
   int issued = 0;
   auto issue_pending = [&]() {
