@@ -11,6 +11,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import paged_kv_cache_186_gb300 as pa
 import workloads as W
 from gpu_util import assert_attention_close, host_subproblem, oracle_store_and_decode, to_device
@@ -156,3 +157,27 @@ def test_append_full_size_workload(name):
     got = assert_same_as_separate(g, max_context_len=max(lens))
     want = oracle_store_and_decode(h)
     assert_attention_close(got[seqs], want, name)
+
+
+def test_back_to_back_calls_see_lengths_and_tables_rewritten_in_between():
+    # Decode launches let the next one start early and read context_lens and
+    # block_tables before waiting. Rewriting both on the device (ordinary
+    # kernels) between two calls, with no host synchronisation, must still be
+    # seen by the second call.
+    lens = [40, 700, 1500, 33]
+    h = W.make_decode(len(lens), 32, 8, 128, 16, lens, seed=170)
+    g = to_device(h)
+    pa.decode_append(g.q, g.k_new, g.v_new, g.k_cache, g.v_cache, g.block_tables,
+                     g.context_lens, g.scale)
+    g.context_lens[1:2].fill_(300)  # shorten one sequence
+    n2 = (lens[2] + 15) // 16
+    g.block_tables[2, :n2] = g.block_tables[2, :n2].flip(0)  # reorder another's blocks
+    out = pa.decode(g.q, g.k_cache, g.v_cache, g.block_tables, g.context_lens, g.scale)
+    torch.cuda.synchronize()
+    assert pa.get_device_error() == 0
+    # the oracle over the same (appended) cache with the rewritten inputs
+    want = oracle.decode(W.bf16_bits(g.q.cpu()), W.bf16_bits(g.k_cache.cpu()),
+                         W.bf16_bits(g.v_cache.cpu()), g.block_tables.cpu().numpy(),
+                         g.context_lens.cpu().numpy(), g.scale)
+    assert int(g.context_lens[1]) == 300
+    assert_attention_close(out, want, "rewritten lengths/tables")
