@@ -494,11 +494,17 @@ __device__ __forceinline__ void write_warp_result(const DecodeArgs& a, int b, in
 // Warps that take part: one per kBlocksPerWarp blocks of work (fewer pieces
 // and merges; measured best from batch 4 to 64 at ~2k tokens), but at least
 // one per kMinBlocksPerWarp blocks up to one warp per CTA, so that small
-// problems keep some parallelism. Every active warp owns a non-empty range.
+// problems keep some parallelism, and at most kMaxPartsPerSegment per
+// (sequence, kv head) segment, so that the last arriver of a long segment
+// does not merge hundreds of partials (one 100k-token sequence: 179 -> 112
+// us). Every active warp owns a non-empty range.
 constexpr int kBlocksPerWarp = 16;
 constexpr int kMinBlocksPerWarp = 4;
-__device__ __forceinline__ long long active_warps(long long N, long long ctas, long long warps) {
-  const long long w = max(N / kBlocksPerWarp, min(N / kMinBlocksPerWarp, ctas));
+constexpr int kMaxPartsPerSegment = 64;
+__device__ __forceinline__ long long active_warps(long long N, long long ctas, long long warps,
+                                                  long long segments) {
+  long long w = max(N / kBlocksPerWarp, min(N / kMinBlocksPerWarp, ctas));
+  w = min(w, segments * kMaxPartsPerSegment);
   return max(1LL, min(warps, w));
 }
 
@@ -768,7 +774,8 @@ __global__ void __launch_bounds__(NW * 32, 3)
 
   // ---- this warp's range; from here on warps are independent
   const long long N = static_cast<long long>(prefix[B]) * Hkv;
-  const long long W = active_warps(N, gridDim.x, static_cast<long long>(gridDim.x) * NW);
+  const long long W = active_warps(N, gridDim.x, static_cast<long long>(gridDim.x) * NW,
+                                   static_cast<long long>(B) * Hkv);
   const long long gw = static_cast<long long>(blockIdx.x) * NW + warp;
   const long long r0 = gw < W ? gw * N / W : 0, r1 = gw < W ? (gw + 1) * N / W : 0;
   const bool active = r0 < r1;  // warps past W (or with an empty range) only wait
