@@ -312,6 +312,7 @@ pa_status decode_common(const void* q, const pa_kv_cache* cache, const int32_t* 
     // 8-byte aligned arrival counters after the prefix sums
     const uintptr_t cp = reinterpret_cast<uintptr_t>(a.prefix_out + batch + 1);
     a.seg_counters = reinterpret_cast<unsigned long long*>((cp + 15) & ~static_cast<uintptr_t>(15));
+    a.grp_counters = a.seg_counters + static_cast<size_t>(batch) * cache->num_kv_heads;
     a.epoch = next_epoch();
   }
   a.err = dev->err;

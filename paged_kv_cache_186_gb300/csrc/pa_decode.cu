@@ -495,12 +495,12 @@ __device__ __forceinline__ void write_warp_result(const DecodeArgs& a, int b, in
 // and merges; measured best from batch 4 to 64 at ~2k tokens), but at least
 // one per kMinBlocksPerWarp blocks up to one warp per CTA, so that small
 // problems keep some parallelism, and at most kMaxPartsPerSegment per
-// (sequence, kv head) segment, so that the last arriver of a long segment
-// does not merge hundreds of partials (one 100k-token sequence: 179 -> 112
-// us). Every active warp owns a non-empty range.
+// (sequence, kv head) segment. Segments of more than kMergeGroup parts merge
+// in two levels, so no warp merges more than kMergeGroup + the number of
+// groups partials. Every active warp owns a non-empty range.
 constexpr int kBlocksPerWarp = 16;
 constexpr int kMinBlocksPerWarp = 4;
-constexpr int kMaxPartsPerSegment = 64;
+constexpr int kMaxPartsPerSegment = 1024;
 __device__ __forceinline__ long long active_warps(long long N, long long ctas, long long warps,
                                                   long long segments) {
   long long w = max(N / kBlocksPerWarp, min(N / kMinBlocksPerWarp, ctas));
@@ -517,6 +517,18 @@ struct SegParts {
   __device__ __forceinline__ long long slot(int j) const {
     return j == 0 ? 2 * w0 + 1 : 2 * (w0 + j);
   }
+};
+
+// Long segments merge in two levels: parts [16 g, 16 g + 16) form group g;
+// the last arriver of a group merges it into the slot of the group's first
+// part, and the last group to finish merges the group results.
+constexpr int kMergeGroup = 16;
+
+// Parts j0, j0 + stride, ... (n of them) of a segment, for a merge.
+struct PartList {
+  SegParts sp;
+  int j0, stride, n;
+  __device__ __forceinline__ long long slot(int k) const { return sp.slot(j0 + k * stride); }
 };
 
 __device__ __forceinline__ SegParts seg_parts(const int* prefix, int B, int Hkv, int b, int kvh,
@@ -555,16 +567,21 @@ __device__ __forceinline__ uint32_t tagged_fetch_add(unsigned long long* counter
   return 0xffffffffu;
 }
 
-// Tag counters [lo, hi) with this call's epoch and a zero count, unless
-// already tagged (one lane per counter).
+// Tag segment counters [lo, hi) and, unless `grp` is null, the two group
+// counters grp[0..1] with this call's epoch and a zero count, unless already
+// tagged (one lane per counter).
 __device__ __forceinline__ void tag_counters(unsigned long long* counters, long long lo,
-                                             long long hi, uint32_t epoch, int lane) {
+                                             long long hi, unsigned long long* grp, uint32_t epoch,
+                                             int lane) {
   const unsigned long long tagged = static_cast<unsigned long long>(epoch) << 32;
-  for (long long i = lo + lane; i < hi; i += 32) {
-    unsigned long long cur = atomicAdd(counters + i, 0ull);
+  const int ng = grp != nullptr ? 2 : 0;
+  const long long n = ng + max(hi - lo, 0LL);
+  for (long long k = lane; k < n; k += 32) {
+    unsigned long long* const c = k < ng ? grp + k : counters + lo + (k - ng);
+    unsigned long long cur = atomicAdd(c, 0ull);
 #pragma unroll 1
     for (int it = 0; it < 8 && static_cast<uint32_t>(cur >> 32) != epoch; ++it) {
-      const unsigned long long prev = atomicCAS(counters + i, cur, tagged);
+      const unsigned long long prev = atomicCAS(c, cur, tagged);
       if (prev == cur) break;
       cur = prev;
     }
@@ -577,16 +594,17 @@ __device__ __forceinline__ bool arrive_last(unsigned long long* counter, uint32_
   return tagged_fetch_add(counter, epoch, err) + 1u == parts;
 }
 
-// Merge the partials of segment (b, kvh) and write its bf16 rows:
-// M = max m_j, l = sum l_j 2^(m_j - M), o = sum o_j 2^(m_j - M) / l (scores in
-// base 2), for all G heads at once. Lane = (part j, head g) with GP lanes per
-// part (G rounded up to a power of two): one round of loads gives every
-// (max, sum), combined online within a lane and across lanes by shuffles;
-// then each lane accumulates D/32 dims of every head over the parts with
-// independent loads. Partials are read through L2.
+// Merge partials of segment (b, kvh): M = max m_j, l = sum l_j 2^(m_j - M),
+// o = sum o_j 2^(m_j - M) (scores in base 2), for all G heads at once. With
+// `final_out` the bf16 rows o / l are written; otherwise (M, l, o) is stored
+// as one partial in the slot of the list's first part. Lane = (part j, head
+// g) with GP lanes per part (G rounded up to a power of two): one round of
+// loads gives every (max, sum), combined online within a lane and across
+// lanes by shuffles; then each lane accumulates D/32 dims of every head over
+// the parts with independent loads. Partials are read through L2.
 template <int D, int GP>
-__device__ __forceinline__ void merge_segment_g(const DecodeArgs& a, const SegParts& sp, int b,
-                                                int kvh, int lane) {
+__device__ __forceinline__ void merge_segment_g(const DecodeArgs& a, const PartList& sp, int b,
+                                                int kvh, bool final_out, int lane) {
   constexpr int V = D / 32;
   constexpr int PR = 32 / GP;  // parts per round
   const int G = a.group;
@@ -641,6 +659,23 @@ __device__ __forceinline__ void merge_segment_g(const DecodeArgs& a, const SegPa
       }
     }
   }
+  if (!final_out) {
+    // one partial of the merged parts, in the slot of the first of them
+    const long long slot = sp.slot(0);
+    if (j_l == 0 && g_ok) {
+      a.part_ml[(slot * GP + g_l) * 2 + 0] = M;
+      a.part_ml[(slot * GP + g_l) * 2 + 1] = L;
+    }
+#pragma unroll
+    for (int g = 0; g < GP; ++g) {
+      if (g < G) {
+        float* dst = a.part_o + (slot * GP + g) * D + lane * V;
+#pragma unroll
+        for (int v = 0; v < V; ++v) dst[v] = acc[g][v];
+      }
+    }
+    return;
+  }
 #pragma unroll
   for (int g = 0; g < GP; ++g) {
     const float lg = __shfl_sync(kFull, L, g);
@@ -657,12 +692,38 @@ __device__ __forceinline__ void merge_segment_g(const DecodeArgs& a, const SegPa
 }
 
 template <int D>
-__device__ __forceinline__ void merge_segment(const DecodeArgs& a, const SegParts& sp, int b,
-                                              int kvh, int lane) {
-  if (a.group <= 1) merge_segment_g<D, 1>(a, sp, b, kvh, lane);
-  else if (a.group <= 2) merge_segment_g<D, 2>(a, sp, b, kvh, lane);
-  else if (a.group <= 4) merge_segment_g<D, 4>(a, sp, b, kvh, lane);
-  else merge_segment_g<D, 8>(a, sp, b, kvh, lane);
+__device__ __forceinline__ void merge_segment(const DecodeArgs& a, const PartList& sp, int b,
+                                              int kvh, bool final_out, int lane) {
+  if (a.group <= 1) merge_segment_g<D, 1>(a, sp, b, kvh, final_out, lane);
+  else if (a.group <= 2) merge_segment_g<D, 2>(a, sp, b, kvh, final_out, lane);
+  else if (a.group <= 4) merge_segment_g<D, 4>(a, sp, b, kvh, final_out, lane);
+  else merge_segment_g<D, 8>(a, sp, b, kvh, final_out, lane);
+}
+
+// Arrival of one part of a segment of more than kMergeGroup parts: this
+// part's group first (the group's last arriver merges it into the slot of the
+// group's first part), then the segment over the group results. Out of line:
+// it is rare and must not add registers to the block loop.
+template <int D>
+__device__ __noinline__ void finish_grouped(const DecodeArgs a, const SegParts sp, int b, int kvh,
+                                            long long gw, int lane) {
+  const int j = static_cast<int>(gw - sp.w0), g0 = j - j % kMergeGroup;
+  const int ng = min(kMergeGroup, sp.n - g0);
+  int last = 0;
+  if (lane == 0)
+    last = arrive_last(a.grp_counters + sp.slot(g0), a.epoch, static_cast<uint32_t>(ng), a.err);
+  if (!__shfl_sync(kFull, last, 0)) return;
+  __threadfence();
+  merge_segment<D>(a, PartList{sp, g0, 1, ng}, b, kvh, false, lane);
+  __threadfence();
+  __syncwarp();
+  const int ngroups = (sp.n + kMergeGroup - 1) / kMergeGroup;
+  if (lane == 0)
+    last = arrive_last(a.seg_counters + static_cast<long long>(b) * a.num_kv_heads + kvh, a.epoch,
+                       static_cast<uint32_t>(ngroups), a.err);
+  if (!__shfl_sync(kFull, last, 0)) return;
+  __threadfence();
+  merge_segment<D>(a, PartList{sp, 0, kMergeGroup, ngroups}, b, kvh, true, lane);
 }
 
 template <int D, int BS, int NW, int ST, bool Q8>
@@ -726,6 +787,7 @@ __global__ void __launch_bounds__(NW * 32, 3)
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bars[NW * ST];
   __shared__ int warp_sums[NW];
+  __shared__ int warp_max[NW];
 
   const uint32_t raw = smem_addr(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -745,13 +807,14 @@ __global__ void __launch_bounds__(NW * 32, 3)
   grid_launch_dependents();
 
   // ---- blocks per sequence and their exclusive prefix sum (whole CTA)
-  int carry = 0;
+  int carry = 0, vmax = 0;
   for (int base_i = 0; base_i < B; base_i += NW * 32) {
     const int i = base_i + threadIdx.x;
     int v = 0;
     if (i < B)
       v = seq_window<BS>(min(max(a.context_lens[i], 0), a.len_cap), WIN ? a.window : 0, a.sinks)
               .nvis;
+    vmax = max(vmax, v);
     int incl = v;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -770,7 +833,12 @@ __global__ void __launch_bounds__(NW * 32, 3)
     __syncthreads();
   }
   if (threadIdx.x == 0) prefix[B] = carry;
+  vmax = __reduce_max_sync(kFull, vmax);
+  if (lane == 0) warp_max[warp] = vmax;
   __syncthreads();
+  int max_blk = 0;  // blocks of the longest sequence
+#pragma unroll
+  for (int w = 0; w < NW; ++w) max_blk = max(max_blk, warp_max[w]);
 
   // ---- this warp's range; from here on warps are independent
   const long long N = static_cast<long long>(prefix[B]) * Hkv;
@@ -779,6 +847,9 @@ __global__ void __launch_bounds__(NW * 32, 3)
   const long long gw = static_cast<long long>(blockIdx.x) * NW + warp;
   const long long r0 = gw < W ? gw * N / W : 0, r1 = gw < W ? (gw + 1) * N / W : 0;
   const bool active = r0 < r1;  // warps past W (or with an empty range) only wait
+  // a segment of nblk blocks has at most (nblk - 1) W / N + 2 parts: only
+  // with a segment of more than kMergeGroup parts are the group counters used
+  const bool may_group = static_cast<long long>(max_blk - 1) * W >= (kMergeGroup - 1) * N;
 
   const uint32_t bar0 = smem_addr(&bars[warp * ST]);
   const uint32_t stage0 = base + warp * ST * C::kStage;
@@ -879,7 +950,8 @@ __global__ void __launch_bounds__(NW * 32, 3)
     // segment arrival counters
     const long long nctr = static_cast<long long>(B) * Hkv;
     const long long per = (nctr + W - 1) / W;
-    tag_counters(a.seg_counters, gw * per, min(nctr, (gw + 1) * per), a.epoch, lane);
+    tag_counters(a.seg_counters, gw * per, min(nctr, (gw + 1) * per),
+                 may_group ? a.grp_counters + 2 * gw : nullptr, a.epoch, lane);
   }
 
   // ---- consumer: pieces in order
@@ -928,13 +1000,17 @@ __global__ void __launch_bounds__(NW * 32, 3)
       __threadfence();
       __syncwarp();
       const SegParts sp = seg_parts(prefix, B, Hkv, cp.b, cp.kvh, W);
-      int last = 0;
-      if (lane == 0)
-        last = arrive_last(a.seg_counters + static_cast<long long>(cp.b) * Hkv + cp.kvh, a.epoch,
-                           static_cast<uint32_t>(sp.n), a.err);
-      if (__shfl_sync(kFull, last, 0)) {
-        __threadfence();
-        merge_segment<D>(a, sp, cp.b, cp.kvh, lane);
+      if (sp.n > kMergeGroup) {
+        finish_grouped<D>(a, sp, cp.b, cp.kvh, gw, lane);
+      } else {
+        int last = 0;
+        if (lane == 0)
+          last = arrive_last(a.seg_counters + static_cast<long long>(cp.b) * Hkv + cp.kvh, a.epoch,
+                             static_cast<uint32_t>(sp.n), a.err);
+        if (__shfl_sync(kFull, last, 0)) {
+          __threadfence();
+          merge_segment<D>(a, PartList{sp, 0, 1, sp.n}, cp.b, cp.kvh, true, lane);
+        }
       }
     }
     piece_next(cp, prefix, B, Hkv, r1);
@@ -1247,11 +1323,11 @@ DecodePlan plan_decode(int batch, int num_heads, int num_kv_heads, int head_dim,
     const int group = std::max(1, num_heads / std::max(1, num_kv_heads));
     p.slot_rows = group <= 1 ? 1 : group <= 2 ? 2 : group <= 4 ? 4 : 8;
     const size_t slot_floats = static_cast<size_t>(p.slot_rows) * (head_dim + 2);
-    // partials, prefix sums, 16-byte pad, segment arrival counters
+    // partials, prefix sums, 16-byte pad, segment and group arrival counters
     p.workspace_bytes = p.partial_slots * slot_floats * sizeof(float) +
                         (static_cast<size_t>(batch) + 1) * sizeof(int) + 16 +
                         static_cast<size_t>(batch) * num_kv_heads * sizeof(unsigned long long) +
-                        256;
+                        p.partial_slots * sizeof(unsigned long long) + 256;
     return p;
   }
   p.persistent_ctas = 0;

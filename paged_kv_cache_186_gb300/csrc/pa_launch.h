@@ -54,6 +54,7 @@ struct DecodeArgs {
   float* part_ml;             // (slots, 8, 2) fp32: (max, sum) per head
   int* prefix_out;            // persistent path: (B+1) block prefix sums
   unsigned long long* seg_counters;  // persistent path: (B*Hkv) arrival counters
+  unsigned long long* grp_counters;  // persistent path: one per partial slot (merge groups)
   uint32_t epoch;             // persistent path: tag of this call in seg_counters
   int slot_rows;              // rows (query heads) of one partial slot
   uint32_t* err;

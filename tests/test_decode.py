@@ -168,6 +168,21 @@ def test_one_long_sequence_spread_over_all_ctas():
     assert_attention_close(got, want, "one long sequence")
 
 
+@pytest.mark.parametrize("H,Hkv,bs,kv,L", [
+    (32, 8, 16, "bf16", 100000),
+    (8, 1, 16, "bf16", 100003),   # one segment split into hundreds of parts
+    (8, 8, 32, "bf16", 65537),    # group 1
+    (6, 2, 16, "bf16", 50001),    # group 3
+    (64, 8, 32, "fp8", 99999),
+])
+def test_one_long_sequence_merges_in_groups(H, Hkv, bs, kv, L):
+    # far more than 16 warps per (sequence, kv head): partials merge per
+    # group of 16 and then across groups
+    h = W.make_decode(1, H, Hkv, 128, bs, [L], seed=95 + H + bs, kv_dtype=kv)
+    got, want = run_case(h, max_context_len=L)
+    assert_attention_close(got, want, f"one sequence of {L}")
+
+
 def test_batch_above_persistent_limit_uses_grid_split():
     gen = torch.Generator().manual_seed(93)
     lens = torch.randint(1, 40, (2100,), generator=gen).tolist()
