@@ -495,9 +495,10 @@ __device__ __forceinline__ void write_warp_result(const DecodeArgs& a, int b, in
 // and merges; measured best from batch 4 to 64 at ~2k tokens), but at least
 // one per kMinBlocksPerWarp blocks up to one warp per CTA, so that small
 // problems keep some parallelism, and at most kMaxPartsPerSegment per
-// (sequence, kv head) segment. Segments of more than kMergeGroup parts merge
-// in two levels, so no warp merges more than kMergeGroup + the number of
-// groups partials. Every active warp owns a non-empty range.
+// (sequence, kv head) segment. Segments of more than kGroupedAbove parts
+// merge in two levels, so no warp merges more than max(kGroupedAbove,
+// kMergeGroup + the number of groups) partials. Every active warp owns a
+// non-empty range.
 constexpr int kBlocksPerWarp = 16;
 constexpr int kMinBlocksPerWarp = 4;
 constexpr int kMaxPartsPerSegment = 1024;
@@ -519,10 +520,14 @@ struct SegParts {
   }
 };
 
-// Long segments merge in two levels: parts [16 g, 16 g + 16) form group g;
-// the last arriver of a group merges it into the slot of the group's first
-// part, and the last group to finish merges the group results.
+// Segments of more than kGroupedAbove parts merge in two levels: parts
+// [16 g, 16 g + 16) form group g; the last arriver of a group merges it into
+// the slot of the group's first part, and the last group to finish merges
+// the group results. Up to kGroupedAbove parts one merge is faster (one
+// level fewer of arrival and partial round trips): 16-17 parts 45.7 us
+// against 60.0 us with groups, 57-64 parts 111-112 us against 102-103 us.
 constexpr int kMergeGroup = 16;
+constexpr int kGroupedAbove = 32;
 
 // Parts j0, j0 + stride, ... (n of them) of a segment, for a merge.
 struct PartList {
@@ -700,7 +705,7 @@ __device__ __forceinline__ void merge_segment(const DecodeArgs& a, const PartLis
   else merge_segment_g<D, 8>(a, sp, b, kvh, final_out, lane);
 }
 
-// Arrival of one part of a segment of more than kMergeGroup parts: this
+// Arrival of one part of a segment of more than kGroupedAbove parts: this
 // part's group first (the group's last arriver merges it into the slot of the
 // group's first part), then the segment over the group results. Out of line:
 // it is rare and must not add registers to the block loop.
@@ -848,8 +853,9 @@ __global__ void __launch_bounds__(NW * 32, 3)
   const long long r0 = gw < W ? gw * N / W : 0, r1 = gw < W ? (gw + 1) * N / W : 0;
   const bool active = r0 < r1;  // warps past W (or with an empty range) only wait
   // a segment of nblk blocks has at most (nblk - 1) W / N + 2 parts: only
-  // with a segment of more than kMergeGroup parts are the group counters used
-  const bool may_group = static_cast<long long>(max_blk - 1) * W >= (kMergeGroup - 1) * N;
+  // with a segment of more than kGroupedAbove parts are the group counters used
+  const bool may_group =
+      static_cast<long long>(max_blk - 1) * W >= static_cast<long long>(kGroupedAbove - 1) * N;
 
   const uint32_t bar0 = smem_addr(&bars[warp * ST]);
   const uint32_t stage0 = base + warp * ST * C::kStage;
@@ -1000,7 +1006,7 @@ __global__ void __launch_bounds__(NW * 32, 3)
       __threadfence();
       __syncwarp();
       const SegParts sp = seg_parts(prefix, B, Hkv, cp.b, cp.kvh, W);
-      if (sp.n > kMergeGroup) {
+      if (sp.n > kGroupedAbove) {
         finish_grouped<D>(a, sp, cp.b, cp.kvh, gw, lane);
       } else {
         int last = 0;
