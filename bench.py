@@ -263,10 +263,44 @@ def cpu_baseline(name: str, budget_s: float = 15.0, window: int = 0, sinks: int 
     h, lens = oracle_sample(name, n)
     dt = run_oracle_step(h, threads, window, sinks)
     keys = sum(visible_keys(L, window, sinks) for L in lens)
+    # the same on one core, on its own bounded sample
+    n1 = sample_size_for(name, budget_s / 3, 1, window, sinks)
+    h1, lens1 = oracle_sample(name, n1)
+    dt1 = run_oracle_step(h1, 1, window, sinks)
+    total = len(W.workload_lengths(name))
     return {"value": kv_bytes(name, lens, window, sinks) / dt / 1e9, "unit": "GB/s",
             "cores": threads, "kind": "oracle",
-            "sample": f"first {n} of {len(W.workload_lengths(name))} sequences "
-                      f"({keys} attended keys), one store_kv+decode, fp64 C oracle, {dt:.2f} s"}
+            "sample": f"first {n} of {total} sequences "
+                      f"({keys} attended keys), one store_kv+decode, fp64 C oracle, {dt:.2f} s",
+            "value_1core": kv_bytes(name, lens1, window, sinks) / dt1 / 1e9,
+            "sample_1core": f"first {n1} of {total} sequences, one core, {dt1:.2f} s"}
+
+
+def copy_ceiling(dev) -> dict:
+    """A plain device-to-device copy of 1 GiB (torch, not this library): the
+    practical HBM ceiling on this machine beside the kernel's own figure. Read +
+    write bytes over the median of 10 timed copies."""
+    n = 1 << 30
+    src = torch.empty(n, dtype=torch.uint8, device=dev)
+    dst = torch.empty_like(src)
+    src.fill_(1)
+    for _ in range(3):
+        dst.copy_(src)
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(10):
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        dst.copy_(src)
+        e.record()
+        e.synchronize()
+        times.append(s.elapsed_time(e))
+    times.sort()
+    gbs = 2 * n / (times[len(times) // 2] / 1e3) / 1e9
+    del src, dst
+    torch.cuda.empty_cache()
+    return {"copy_gbs": gbs, "what": "torch device-to-device copy of 1 GiB, read+write bytes, "
+                                     "median of 10"}
 
 
 def run_reference(args, world, rank):
@@ -516,6 +550,10 @@ def run_gpu(args, world, rank, local):
         "gpu_launches": n_launch * args.steps,
         "clocks": clocks,
     }
+    if world == 1:
+        ceil = copy_ceiling(dev)
+        ceil["kernel_frac_of_copy"] = achieved / ceil["copy_gbs"]
+        line["ceiling"] = ceil
     if not args.no_cpu_baseline and world == 1:
         line["cpu_baseline"] = cpu_baseline(name, window=win, sinks=snk)
     print(json.dumps(line), flush=True)
