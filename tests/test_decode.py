@@ -183,6 +183,23 @@ def test_one_long_sequence_merges_in_groups(H, Hkv, bs, kv, L):
     assert_attention_close(got, want, f"one sequence of {L}")
 
 
+@pytest.mark.parametrize("H,Hkv,kv,L", [
+    (32, 8, "bf16", 2048),   # 128 blocks per segment: 32 parts, one merge
+    (32, 8, "bf16", 2112),   # 33 parts: groups of 16, 16 and a 1-part tail
+    (32, 8, "bf16", 2176),   # 34 parts: 16, 16, 2
+    (32, 8, "bf16", 2065),   # 130 blocks, the last one partly filled
+    (8, 8, "bf16", 2112),    # group 1
+    (64, 8, "fp8", 2112),
+])
+def test_merge_group_boundaries(H, Hkv, kv, L):
+    # one sequence of fewer than 4 * (persistent CTAs) blocks over all kv
+    # heads: one warp per 4 blocks, so a segment of n blocks has n / 4 parts
+    bs = 32 if kv == "fp8" else 16
+    h = W.make_decode(1, H, Hkv, 128, bs, [L * bs // 16], seed=97 + L + H, kv_dtype=kv)
+    got, want = run_case(h, max_context_len=L * bs // 16)
+    assert_attention_close(got, want, f"one sequence of {L * bs // 16} ({kv})")
+
+
 def test_batch_above_persistent_limit_uses_grid_split():
     gen = torch.Generator().manual_seed(93)
     lens = torch.randint(1, 40, (2100,), generator=gen).tolist()
