@@ -10,7 +10,12 @@ unless --workload says otherwise.
 Prints ONE JSON line (rank 0). Inputs are resident in HBM before timing; the
 step rotates over several independently drawn KV pools so consecutive steps
 never re-read KV from L2. The decode launch is also timed on its own with CUDA
-events inside the timed region for the roofline figure.
+events inside the timed region for the roofline figure. The default run also
+measures the other workloads (the tiny decode, the long-context decode with
+and without a sliding window, the FP8 and INT8 70B-shaped decodes and the
+varlen prefill) in the same process and adds them to the line under
+"workloads", each with its own oracle baseline and clock record
+(--headline-only skips them).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
   python bench.py --impl reference ...   # the CPU oracle as the reference arm
@@ -255,7 +260,8 @@ def sample_size_for(name: str, budget_s: float, threads: int, window: int = 0,
     return max(1, n)
 
 
-def cpu_baseline(name: str, budget_s: float = 15.0, window: int = 0, sinks: int = 0):
+def cpu_baseline(name: str, budget_s: float = 15.0, window: int = 0, sinks: int = 0,
+                 one_core: bool = True):
     import oracle
     oracle.build()
     threads = len(os.sched_getaffinity(0))
@@ -263,17 +269,72 @@ def cpu_baseline(name: str, budget_s: float = 15.0, window: int = 0, sinks: int 
     h, lens = oracle_sample(name, n)
     dt = run_oracle_step(h, threads, window, sinks)
     keys = sum(visible_keys(L, window, sinks) for L in lens)
-    # the same on one core, on its own bounded sample
-    n1 = sample_size_for(name, budget_s / 3, 1, window, sinks)
-    h1, lens1 = oracle_sample(name, n1)
-    dt1 = run_oracle_step(h1, 1, window, sinks)
     total = len(W.workload_lengths(name))
-    return {"value": kv_bytes(name, lens, window, sinks) / dt / 1e9, "unit": "GB/s",
-            "cores": threads, "kind": "oracle",
-            "sample": f"first {n} of {total} sequences "
-                      f"({keys} attended keys), one store_kv+decode, fp64 C oracle, {dt:.2f} s",
-            "value_1core": kv_bytes(name, lens1, window, sinks) / dt1 / 1e9,
-            "sample_1core": f"first {n1} of {total} sequences, one core, {dt1:.2f} s"}
+    res = {"value": kv_bytes(name, lens, window, sinks) / dt / 1e9, "unit": "GB/s",
+           "cores": threads, "kind": "oracle",
+           "sample": f"first {n} of {total} sequences "
+                     f"({keys} attended keys), one store_kv+decode, fp64 C oracle, {dt:.2f} s"}
+    if one_core:
+        # the same on one core, on its own bounded sample
+        n1 = sample_size_for(name, budget_s / 3, 1, window, sinks)
+        h1, lens1 = oracle_sample(name, n1)
+        dt1 = run_oracle_step(h1, 1, window, sinks)
+        res["value_1core"] = kv_bytes(name, lens1, window, sinks) / dt1 / 1e9
+        res["sample_1core"] = f"first {n1} of {total} sequences, one core, {dt1:.2f} s"
+    return res
+
+
+def prefill_oracle_sample(name: str, max_seqs: int, seed: int = 0):
+    """Host inputs of the first `max_seqs` sequences of a prefill workload
+    (same cached and new lengths, shapes and value recipe)."""
+    w = W.WORKLOADS[name]
+    cached, qls = W.prefill_lengths(name)
+    cached, qls = cached[:max_seqs], qls[:max_seqs]
+    h = W.make_prefill(len(qls), w["num_heads"], w["num_kv_heads"], w["head_dim"],
+                       w["block_size"], cached, qls, pool_factor=w["pool_factor"],
+                       seed=w["seed"] + 7 + seed, scale=w["scale"])
+    return h, cached, qls
+
+
+def run_oracle_prefill_step(h, threads: int) -> float:
+    import oracle
+    kc, vc = W.bf16_bits(h.k_cache).copy(), W.bf16_bits(h.v_cache).copy()
+    t0 = time.perf_counter()
+    oracle.store_kv(W.bf16_bits(h.k_new), W.bf16_bits(h.v_new), h.slot_mapping.numpy(), kc, vc)
+    oracle.prefill(W.bf16_bits(h.q), kc, vc, h.block_tables.numpy(), h.cu_seqlens_q.numpy(),
+                   h.cu_seqlens_k.numpy(), h.scale, threads=threads)
+    return time.perf_counter() - t0
+
+
+def prefill_sample_size(name: str, budget_s: float, threads: int) -> int:
+    """Sequences per oracle prefill step so one step takes about budget_s
+    (estimated from a 1-sequence probe, by FLOPs)."""
+    w = W.WORKLOADS[name]
+    h, cached, qls = prefill_oracle_sample(name, 1)
+    dt = max(run_oracle_prefill_step(h, threads), 1e-4)
+    per_flop = dt / max(1, prefill_flops(cached, qls, w["num_heads"], w["head_dim"]))
+    n, acc = 0, 0.0
+    for c, q in zip(*W.prefill_lengths(name)):
+        cost = prefill_flops([c], [q], w["num_heads"], w["head_dim"]) * per_flop
+        if n > 0 and acc + cost > budget_s:
+            break
+        acc += cost
+        n += 1
+    return max(1, n)
+
+
+def cpu_prefill_baseline(name: str, budget_s: float = 10.0):
+    import oracle
+    oracle.build()
+    w = W.WORKLOADS[name]
+    threads = len(os.sched_getaffinity(0))
+    n = prefill_sample_size(name, budget_s, threads)
+    h, cached, qls = prefill_oracle_sample(name, n)
+    dt = run_oracle_prefill_step(h, threads)
+    flops = prefill_flops(cached, qls, w["num_heads"], w["head_dim"])
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "sample": f"first {n} of {w['batch']} sequences ({sum(qls)} query rows), one "
+                      f"store_kv+prefill, fp64 C oracle, {dt:.2f} s"}
 
 
 def copy_ceiling(dev) -> dict:
@@ -342,7 +403,288 @@ def run_reference(args, world, rank):
     print(json.dumps(line), flush=True)
 
 
+def run_reference_prefill(args, world, rank):
+    """The oracle's prefill (fp64 C, all host cores) on a bounded sample of the
+    varlen prefill workload: its first sequences."""
+    name = args.workload
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    threads = len(os.sched_getaffinity(0))
+    budget = max(0.5, 120.0 / max(1, args.steps + args.warmup))
+    n = prefill_sample_size(name, budget, threads)
+    h, cached, qls = prefill_oracle_sample(name, n)
+    for _ in range(args.warmup):
+        run_oracle_prefill_step(h, threads)
+    t = 0.0
+    for _ in range(args.steps):
+        t += run_oracle_prefill_step(h, threads)
+    per_step = t / max(1, args.steps)
+    w = W.WORKLOADS[name]
+    flops = prefill_flops(cached, qls, w["num_heads"], w["head_dim"])
+    value = flops / per_step / 1e12
+    line = {
+        "impl": "reference", "metric": "Varlen prefix-cached prefill attention TFLOP/s",
+        "value": value, "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": per_step * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": name, "batch": n, "num_heads": w["num_heads"],
+                   "num_kv_heads": w["num_kv_heads"], "head_dim": w["head_dim"],
+                   "block_size": w["block_size"], "q_lens": qls, "cached": cached,
+                   "sample_of_batch": f"{n}/{w['batch']}"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": f"first {n} of {w['batch']} sequences per step"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
 # ------------------------------------------------------------------ GPU arm
+# The other configurations, measured in the default run beside the headline
+# decode (each with its own oracle baseline and clock record): (key, workload,
+# sliding window, sinks).
+OTHER_WORKLOADS = (
+    ("tiny_decode", "tiny_decode", 0, 0),
+    ("long_context_decode_b8", "long_context_decode_b8", 0, 0),
+    ("long_context_decode_b8_window4096_sinks4", "long_context_decode_b8", 4096, 4),
+    ("llama3_70b_fp8_decode_b256", "llama3_70b_fp8_decode_b256", 0, 0),
+    ("llama3_70b_int8_decode_b256", "llama3_70b_int8_decode_b256", 0, 0),
+    ("varlen_prefill_b8", "varlen_prefill_b8", 0, 0),
+)
+
+
+class DecodeBench:
+    """One decode workload on the device: rotating KV pools (so consecutive
+    steps never find the KV in L2), the step as the library's user makes it,
+    device-timed and end-to-end loops."""
+
+    def __init__(self, pa, name, dev, rank=0, window=0, sinks=0, step_kind="append"):
+        self.pa, self.name, self.dev = pa, name, dev
+        self.w = w = W.WORKLOADS[name]
+        self.lens = W.workload_lengths(name)
+        self.B = w["batch"]
+        self.window, self.sinks = window, sinks
+        self.step_bytes = kv_bytes(name, self.lens, window, sinks)
+        self.n_pools = max(2, min(4, math.ceil(4 * L2_BYTES / max(1, self.step_bytes)) + 1))
+        self.pools = [W.make_workload(name, device=dev, variant=v + 97 * rank)
+                      for v in range(self.n_pools)]
+        self.q8 = w["kv_dtype"] in ("fp8", "int8")  # 8-bit codes with scales
+        self.max_len = max(self.lens)
+        p0 = self.pools[0]
+        ws = pa.decode_workspace_size(p0.k_cache, self.B, w["num_heads"],
+                                      p0.block_tables.shape[1], self.max_len,
+                                      k_scale=p0.k_scale, v_scale=p0.v_scale)
+        self.workspace = torch.empty(max(ws, 16), dtype=torch.uint8, device=dev)
+        self.out = torch.empty((self.B, w["num_heads"], w["head_dim"]), dtype=torch.bfloat16,
+                               device=dev)
+        self.stream = torch.cuda.current_stream()
+        # the fused append has no window variant
+        self.fused = step_kind == "append" and window <= 0
+        # store_kv + decode (or the fused append: one persistent launch); the
+        # grid-split path (batches above 2048) adds a merge
+        self.launches_per_step = (1 if self.fused else 2) if self.B <= 2048 else 3
+
+    def describe_step(self):
+        if self.fused:
+            return "decode_append (store of the new tokens fused into decode)"
+        if self.window > 0:
+            return f"store_kv(new tokens) + decode_window(window {self.window}, sinks {self.sinks})"
+        return "store_kv(new tokens) + decode"
+
+    def run(self, p, inp=None, out=None, ev=None):
+        """One step on pool p's cache; step inputs from `inp` (default: p)."""
+        pa, x = self.pa, (p.__dict__ if inp is None else inp)
+        out = self.out if out is None else out
+        if self.fused:
+            if ev is not None:
+                ev[0].record(self.stream)
+            pa.decode_append(x["q"], x["k_new"], x["v_new"], p.k_cache, p.v_cache,
+                             x["block_tables"], x["context_lens"], p.scale,
+                             max_context_len=self.max_len, out=out, workspace=self.workspace,
+                             k_scale_new=x.get("k_scale_new"), v_scale_new=x.get("v_scale_new"),
+                             k_scale=p.k_scale, v_scale=p.v_scale)
+            if ev is not None:
+                ev[1].record(self.stream)
+            return
+        pa.store_kv(x["k_new"], x["v_new"], x["slot_mapping"], p.k_cache, p.v_cache,
+                    x.get("k_scale_new"), x.get("v_scale_new"), p.k_scale, p.v_scale)
+        if ev is not None:
+            ev[0].record(self.stream)
+        pa.decode_window(x["q"], p.k_cache, p.v_cache, x["block_tables"], x["context_lens"],
+                         p.scale, self.window, self.sinks, max_context_len=self.max_len, out=out,
+                         workspace=self.workspace, k_scale=p.k_scale, v_scale=p.v_scale)
+        if ev is not None:
+            ev[1].record(self.stream)
+
+    def warm(self, n):
+        for i in range(n):
+            self.run(self.pools[i % self.n_pools])
+        torch.cuda.synchronize()
+        if self.pa.get_device_error() != 0:
+            raise RuntimeError(f"{self.name}: device error during warm-up")
+
+    def time_device(self, steps, world=1):
+        """Region events around `steps` steps (the fused step is one launch;
+        otherwise the decode launch is also timed on its own). Returns
+        (region ms, decode ms per step, wall start, wall end)."""
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(steps)]
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(world)
+        torch.cuda.synchronize()
+        t0 = time.time()
+        start.record(self.stream)
+        for i in range(steps):
+            # events between launches would add a gap to every fused step
+            self.run(self.pools[i % self.n_pools], ev=None if self.fused else evs[i])
+        end.record(self.stream)
+        torch.cuda.synchronize()
+        t1 = time.time()
+        barrier(world)
+        ms_total = start.elapsed_time(end)
+        if self.fused:
+            dec_ms = ms_total / steps
+        else:
+            dec_ms = sum(a.elapsed_time(b) for a, b in evs) / steps
+        err = self.pa.get_device_error()
+        if err != 0:
+            raise RuntimeError(f"{self.name}: device error word {err:#x} after the timed region")
+        return ms_total, dec_ms, t0, t1
+
+    def time_e2e(self, steps, warmup, world=1):
+        """End to end through the public API with host buffers: each step
+        uploads its inputs (q, new K/V rows, block tables, lengths; packed in
+        one pinned staging buffer per pool: one copy) and downloads its
+        output, over the same rotating pools as the device loop. Two device
+        slots and an upload and a download stream let step i+1's upload and
+        step i-1's download overlap step i's kernels; every step's own copies
+        are inside the timed region. Returns (ms, h2d bytes, d2h bytes)."""
+        dev, stream = self.dev, self.stream
+        keys = ("q", "k_new", "v_new", "block_tables", "context_lens")
+        if not self.fused:
+            keys += ("slot_mapping",)
+        if self.q8:
+            keys += ("k_scale_new", "v_scale_new")
+        p0 = self.pools[0]
+        fields, off = [], 0
+        for k in keys:
+            t = getattr(p0, k)
+            nbytes = t.numel() * t.element_size()
+            fields.append((k, off, nbytes, t.dtype, tuple(t.shape)))
+            off = (off + nbytes + 255) // 256 * 256
+        h2d = off
+        host = []
+        for p in self.pools:
+            buf = torch.empty(h2d, dtype=torch.uint8).pin_memory()
+            for k, o, n, dt, shp in fields:
+                buf[o:o + n].copy_(getattr(p, k).contiguous().cpu().view(-1).view(torch.uint8))
+            host.append(buf)
+        slots = [torch.empty(h2d, dtype=torch.uint8, device=dev) for _ in range(2)]
+        views = [{k: sl[o:o + n].view(dt).view(shp) for k, o, n, dt, shp in fields}
+                 for sl in slots]
+        outs = [torch.empty_like(self.out) for _ in range(2)]
+        out_host = [torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory()
+                    for _ in range(2)]
+        d2h = out_host[0].numel() * out_host[0].element_size()
+        up, down = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+        ev = {k: [torch.cuda.Event() for _ in range(2)] for k in ("in", "used", "out")}
+
+        def e2e_step(i):
+            s, p = i % 2, self.pools[i % self.n_pools]
+            with torch.cuda.stream(up):
+                if i >= 2:
+                    up.wait_event(ev["used"][s])  # step i-2 finished reading slot s
+                slots[s].copy_(host[i % self.n_pools], non_blocking=True)
+                ev["in"][s].record(up)
+            stream.wait_event(ev["in"][s])
+            if i >= 2:
+                stream.wait_event(ev["out"][s])  # step i-2's output has been downloaded
+            self.run(p, inp=views[s], out=outs[s])
+            ev["used"][s].record(stream)
+            with torch.cuda.stream(down):
+                down.wait_event(ev["used"][s])
+                out_host[s].copy_(outs[s], non_blocking=True)
+                ev["out"][s].record(down)
+
+        for i in range(max(3, warmup)):
+            e2e_step(i)
+        torch.cuda.synchronize()
+        e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(world)
+        torch.cuda.synchronize()
+        e_start.record(stream)
+        up.wait_event(e_start)
+        for i in range(steps):
+            e2e_step(i)
+        e_end.record(down)  # after the last download
+        torch.cuda.synchronize()
+        barrier(world)
+        return e_start.elapsed_time(e_end), h2d, d2h
+
+    def config(self):
+        w = self.w
+        return {"workload": self.name, "batch": self.B, "num_heads": w["num_heads"],
+                "num_kv_heads": w["num_kv_heads"], "head_dim": w["head_dim"],
+                "block_size": w["block_size"], "kv_dtype": w["kv_dtype"],
+                "context_len_mean": sum(self.lens) / len(self.lens),
+                "context_len_max": self.max_len, "kv_bytes_per_step": self.step_bytes,
+                **({"window": self.window, "sinks": self.sinks} if self.window > 0 else {}),
+                "step": self.describe_step(),
+                "l2": f"rotating {self.n_pools} KV pools, "
+                      f"{self.n_pools * self.step_bytes / 1e9:.3f} GB of KV between reuses"
+                      + (" > 129 MB L2" if self.n_pools * self.step_bytes > L2_BYTES
+                         else " (fits in the 129 MB L2: launch-bound)")}
+
+    def free(self):
+        del self.pools, self.workspace, self.out
+        torch.cuda.empty_cache()
+
+
+def steps_for_wall(per_step_ms, target_s, lo, hi):
+    """Steps that keep a timed region busy about target_s (for clock samples)."""
+    n = int(target_s * 1e3 / max(per_step_ms, 1e-3))
+    return max(lo, min(hi, n))
+
+
+def other_decode_entry(pa, key, name, dev, args, window, sinks):
+    b = DecodeBench(pa, name, dev, window=window, sinks=sinks, step_kind=args.step)
+    b.warm(max(3, args.warmup))
+    probe, _, _, _ = b.time_device(10)
+    steps = steps_for_wall(probe / 10, 0.5, max(args.steps, 20), 20000)
+    ms_total, dec_ms, t0, t1 = b.time_device(steps)
+    e2e_ms, h2d, d2h = b.time_e2e(steps, args.warmup)
+    peak, peak_kind = peaks()
+    gbs = b.step_bytes / (ms_total / steps / 1e3) / 1e9
+    achieved = b.step_bytes / (dec_ms / 1e3) / 1e9
+    fits_l2 = b.n_pools * b.step_bytes <= L2_BYTES
+    entry = {
+        "kind": "decode", "steps": steps, "us_per_step": ms_total / steps * 1e3,
+        "kv_gbs": gbs, "seq_steps_per_s": b.B * steps / (ms_total / 1e3),
+        "roofline": ({"bound": "launch", "note": "KV of all pools fits in L2: launch-bound "
+                      "latency, no HBM roofline fraction", "achieved": achieved, "unit": "GB/s"}
+                     if fits_l2 else
+                     {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                      "frac": achieved / peak, "peak_kind": f"of {peak_kind}",
+                      "kernel": ("decode_persistent_kernel (pa_decode_append: region events / "
+                                 "steps)" if b.fused else
+                                 "decode_persistent_kernel (pa_decode_window: CUDA events per "
+                                 "call)")}),
+        "e2e": {"value": b.step_bytes * steps / (e2e_ms / 1e3) / 1e9, "unit": "GB/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": b.launches_per_step * steps,
+        "config": b.config(),
+        "_wall": (t0, t1),
+    }
+    b.free()
+    if not args.no_cpu_baseline:
+        entry["cpu_baseline"] = cpu_baseline(name, budget_s=4.0, window=window, sinks=sinks,
+                                             one_core=False)
+    del key
+    return entry
+
+
 def run_gpu(args, world, rank, local):
     import paged_kv_cache_186_gb300 as pa
     from paged_kv_cache_186_gb300 import build as pabuild
@@ -350,191 +692,40 @@ def run_gpu(args, world, rank, local):
         pabuild.build()
     barrier(world)
     name = args.workload
-    w = W.WORKLOADS[name]
     dev = torch.device("cuda", torch.cuda.current_device())
-    lens = W.workload_lengths(name)
-    B = w["batch"]
-    win, snk = args.window, args.sinks
-    step_bytes = kv_bytes(name, lens, win, snk)
-    pool_bytes = step_bytes
-    n_pools = max(2, min(4, math.ceil(4 * L2_BYTES / max(1, pool_bytes)) + 1))
-    pools = [W.make_workload(name, device=dev, variant=v + 97 * rank) for v in range(n_pools)]
-    q8 = w["kv_dtype"] in ("fp8", "int8")  # 8-bit codes with scales
-    max_len = max(lens)
-    ws_bytes = pa.decode_workspace_size(pools[0].k_cache, B, w["num_heads"],
-                                        pools[0].block_tables.shape[1], max_len,
-                                        k_scale=pools[0].k_scale, v_scale=pools[0].v_scale)
-    workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
-    out = torch.empty((B, w["num_heads"], w["head_dim"]), dtype=torch.bfloat16, device=dev)
-    stream = torch.cuda.current_stream()
-
-    fused = args.step == "append" and win <= 0  # the fused append has no window variant
-
-    def step(p, ev=None):
-        if fused:
-            if ev is not None:
-                ev[0].record(stream)
-            pa.decode_append(p.q, p.k_new, p.v_new, p.k_cache, p.v_cache, p.block_tables,
-                             p.context_lens, p.scale, max_context_len=max_len, out=out,
-                             workspace=workspace, k_scale_new=p.k_scale_new,
-                             v_scale_new=p.v_scale_new, k_scale=p.k_scale, v_scale=p.v_scale)
-            if ev is not None:
-                ev[1].record(stream)
-            return
-        pa.store_kv(p.k_new, p.v_new, p.slot_mapping, p.k_cache, p.v_cache, p.k_scale_new,
-                    p.v_scale_new, p.k_scale, p.v_scale)
-        if ev is not None:
-            ev[0].record(stream)
-        pa.decode_window(p.q, p.k_cache, p.v_cache, p.block_tables, p.context_lens, p.scale,
-                         win, snk, max_context_len=max_len, out=out, workspace=workspace,
-                         k_scale=p.k_scale, v_scale=p.v_scale)
-        if ev is not None:
-            ev[1].record(stream)
-
-    for i in range(args.warmup):
-        step(pools[i % n_pools])
-    torch.cuda.synchronize()
-    if pa.get_device_error() != 0:
-        raise RuntimeError("device error during warm-up")
-
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(args.steps)]
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(local) if rank == 0 else None
     if sampler:
         time.sleep(0.3)
-    barrier(world)
-    torch.cuda.synchronize()
-    t_wall0 = time.time()
-    start.record(stream)
-    for i in range(args.steps):
-        # the fused step is a single launch: the region's own events time it
-        # (events between launches would add a gap to every step)
-        step(pools[i % n_pools], None if fused else evs[i])
-    end.record(stream)
-    torch.cuda.synchronize()
-    t_wall1 = time.time()
-    barrier(world)
-    if sampler:
-        time.sleep(0.3)
-        sampler.stop()
-    ms_total = start.elapsed_time(end)
-    if fused:
-        dec_avg_ms = ms_total / args.steps
-    else:
-        dec_ms = [a.elapsed_time(b) for a, b in evs]
-        dec_avg_ms = sum(dec_ms) / len(dec_ms)
-    err = pa.get_device_error()
-    if err != 0:
-        raise RuntimeError(f"device error word {err:#x} after the timed region")
-
-    # ---------------- end to end through the public API with host buffers
-    # Each step uploads its inputs from pinned host memory (packed into one
-    # staging buffer: one copy) and downloads its output. Two device slots and
-    # an upload and a download stream let step i+1's upload and step i-1's
-    # download overlap step i's kernel; every step's own copies are inside the
-    # timed region.
-    p0 = pools[0]
-    host_keys = ("q", "k_new", "v_new", "block_tables", "context_lens")
-    if not fused:
-        host_keys += ("slot_mapping",)
-    if q8:
-        host_keys += ("k_scale_new", "v_scale_new")
-    fields, off = [], 0
-    for k in host_keys:
-        t = getattr(p0, k).contiguous()
-        nbytes = t.numel() * t.element_size()
-        fields.append((k, off, nbytes, t.dtype, tuple(t.shape)))
-        off = (off + nbytes + 255) // 256 * 256
-    h2d = off
-    host_buf = torch.empty(h2d, dtype=torch.uint8).pin_memory()
-    for k, o, n, dt, shp in fields:
-        host_buf[o:o + n].copy_(getattr(p0, k).contiguous().cpu().view(-1).view(torch.uint8))
-    slots = [torch.empty(h2d, dtype=torch.uint8, device=dev) for _ in range(2)]
-    views = [{k: sl[o:o + n].view(dt).view(shp) for k, o, n, dt, shp in fields} for sl in slots]
-    outs = [torch.empty_like(out) for _ in range(2)]
-    out_host = [torch.empty(out.shape, dtype=out.dtype).pin_memory() for _ in range(2)]
-    d2h = out_host[0].numel() * out_host[0].element_size()
-    up_stream, down_stream = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
-    ev = {k: [torch.cuda.Event() for _ in range(2)] for k in ("in", "used", "done", "out")}
-
-    def e2e_step(i, p):
-        s, v = i % 2, views[i % 2]
-        with torch.cuda.stream(up_stream):
-            if i >= 2:
-                up_stream.wait_event(ev["used"][s])  # step i-2 finished reading slot s
-            slots[s].copy_(host_buf, non_blocking=True)
-            ev["in"][s].record(up_stream)
-        stream.wait_event(ev["in"][s])
-        if i >= 2:
-            stream.wait_event(ev["out"][s])  # step i-2's output has been downloaded
-        if fused:
-            pa.decode_append(v["q"], v["k_new"], v["v_new"], p.k_cache, p.v_cache,
-                             v["block_tables"], v["context_lens"], p.scale,
-                             max_context_len=max_len, out=outs[s], workspace=workspace,
-                             k_scale_new=v.get("k_scale_new"), v_scale_new=v.get("v_scale_new"),
-                             k_scale=p.k_scale, v_scale=p.v_scale)
-        else:
-            pa.store_kv(v["k_new"], v["v_new"], v["slot_mapping"], p.k_cache, p.v_cache,
-                        v.get("k_scale_new"), v.get("v_scale_new"), p.k_scale, p.v_scale)
-            pa.decode_window(v["q"], p.k_cache, p.v_cache, v["block_tables"], v["context_lens"],
-                             p.scale, win, snk, max_context_len=max_len, out=outs[s],
-                             workspace=workspace, k_scale=p.k_scale, v_scale=p.v_scale)
-        ev["used"][s].record(stream)
-        ev["done"][s].record(stream)
-        with torch.cuda.stream(down_stream):
-            down_stream.wait_event(ev["done"][s])
-            out_host[s].copy_(outs[s], non_blocking=True)
-            ev["out"][s].record(down_stream)
-
-    for i in range(max(3, args.warmup)):
-        e2e_step(i, p0)
-    torch.cuda.synchronize()
-    e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier(world)
-    torch.cuda.synchronize()
-    e_start.record(stream)
-    up_stream.wait_event(e_start)
-    for i in range(args.steps):
-        e2e_step(i, p0)  # same pool: the KV cache is resident state, only step inputs move
-    e_end.record(down_stream)  # after the last download
-    torch.cuda.synchronize()
-    barrier(world)
-    e2e_ms = e_start.elapsed_time(e_end)
+    b = DecodeBench(pa, name, dev, rank=rank, window=args.window, sinks=args.sinks,
+                    step_kind=args.step)
+    b.warm(args.warmup)
+    ms_total, dec_avg_ms, t_wall0, t_wall1 = b.time_device(args.steps, world)
+    e2e_ms, h2d, d2h = b.time_e2e(args.steps, args.warmup, world)
 
     ms_total = max_over_ranks(world, ms_total)
     e2e_ms = max_over_ranks(world, e2e_ms)
     dec_avg_ms = max_over_ranks(world, dec_avg_ms)
-    total_bytes = sum_over_ranks(world, float(step_bytes)) * args.steps
+    total_bytes = sum_over_ranks(world, float(b.step_bytes)) * args.steps
     value = total_bytes / (ms_total / 1e3) / 1e9
     e2e_value = total_bytes / (e2e_ms / 1e3) / 1e9
+    step_bytes, B, w, fused = b.step_bytes, b.B, b.w, b.fused
+    config = b.config()
+    launches = b.launches_per_step * args.steps
+    b.free()
 
     if rank != 0:
         return
     peak, peak_kind = peaks()
     achieved = step_bytes / (dec_avg_ms / 1e3) / 1e9
-    traffic = traffic_from_profile("pa_decode.cu", name) if win <= 0 else None
-    # store_kv + decode (or the fused append: one persistent launch); the
-    # grid-split path (batches above 2048) adds a merge
-    n_launch = (1 if fused else 2) if B <= 2048 else 3
-    clocks = sampler.summary(t_wall0, t_wall1) if sampler else None
+    traffic = traffic_from_profile("pa_decode.cu", name) if args.window <= 0 else None
+    config["parallelism"] = f"replicas x{world} (sequences sharded, no collective)"
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_total / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": {"fp8": "fp8_e4m3", "int8": "int8"}.get(w["kv_dtype"], "bf16"),
         "data": "synthetic",
-        "config": {"workload": name, "batch": B, "num_heads": w["num_heads"],
-                   "num_kv_heads": w["num_kv_heads"], "head_dim": w["head_dim"],
-                   "block_size": w["block_size"], "kv_dtype": w["kv_dtype"],
-                   "context_len_mean": sum(lens) / len(lens), "context_len_max": max_len,
-                   "kv_bytes_per_step": step_bytes,
-                   **({"window": win, "sinks": snk} if win > 0 else {}),
-                   "step": ("decode_append (store of the new tokens fused into decode)"
-                            if fused else "store_kv(new tokens) + decode"),
-                   "l2": f"rotating {n_pools} KV pools, {n_pools * step_bytes / 1e9:.2f} GB of KV "
-                         f"between reuses > 129 MB L2",
-                   "parallelism": f"replicas x{world} (sequences sharded, no collective)"},
+        "config": config,
         "seq_steps_per_s": B * world * args.steps / (ms_total / 1e3),
         "us_per_step": ms_total / args.steps * 1e3,
         "hbm_frac_of_peak": value / peak,
@@ -547,16 +738,121 @@ def run_gpu(args, world, rank, local):
                      "peak_kind": f"of {peak_kind}"},
         "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
-        "gpu_launches": n_launch * args.steps,
-        "clocks": clocks,
+        "gpu_launches": launches,
+        "clocks": None,
     }
     if world == 1:
         ceil = copy_ceiling(dev)
         ceil["kernel_frac_of_copy"] = achieved / ceil["copy_gbs"]
         line["ceiling"] = ceil
     if not args.no_cpu_baseline and world == 1:
-        line["cpu_baseline"] = cpu_baseline(name, window=win, sinks=snk)
+        line["cpu_baseline"] = cpu_baseline(name, window=args.window, sinks=args.sinks)
+    if world == 1 and not args.headline_only and name == DEFAULT_WORKLOAD and args.window <= 0:
+        others = {}
+        for key, wname, win, snk in OTHER_WORKLOADS:
+            if W.WORKLOADS[wname]["kind"] == "prefill":
+                others[key] = prefill_entry(pa, wname, dev, args)
+            else:
+                others[key] = other_decode_entry(pa, key, wname, dev, args, win, snk)
+        line["workloads"] = others
+    if sampler:
+        time.sleep(0.3)
+        sampler.stop()
+        line["clocks"] = sampler.summary(t_wall0, t_wall1)
+    for e in line.get("workloads", {}).values():
+        wall = e.pop("_wall")
+        e["clocks"] = sampler.summary(*wall) if sampler else None
     print(json.dumps(line), flush=True)
+
+
+class PrefillBench:
+    """The varlen prefill step: store_kv of the new tokens + pa_prefill_varlen,
+    over rotating pools with an L2 flush between steps (the ~52 MB of K/V
+    read per step fits in L2)."""
+
+    def __init__(self, pa, name, dev, rank=0):
+        self.pa, self.name, self.dev = pa, name, dev
+        self.w = w = W.WORKLOADS[name]
+        self.pools = [W.make_workload(name, device=dev, variant=v + 97 * rank) for v in range(3)]
+        m = self.pools[0].meta
+        self.m = m
+        self.flops = prefill_flops(m["cached"], m["q_lens"], w["num_heads"], w["head_dim"])
+        self.max_q = max(m["q_lens"])
+        self.total_q = sum(m["q_lens"])
+        self.out = torch.empty((self.total_q, w["num_heads"], w["head_dim"]),
+                               dtype=torch.bfloat16, device=dev)
+        self.flush = torch.empty(256 * 2 ** 20, dtype=torch.uint8, device=dev)
+        self.stream = torch.cuda.current_stream()
+
+    def run(self, p, ev=None):
+        pa = self.pa
+        pa.store_kv(p.k_new, p.v_new, p.slot_mapping, p.k_cache, p.v_cache)
+        if ev is not None:
+            ev[0].record(self.stream)
+        pa.prefill_varlen(p.q, p.k_cache, p.v_cache, p.block_tables, p.cu_seqlens_q,
+                          p.cu_seqlens_k, p.scale, max_q_len=self.max_q, out=self.out)
+        if ev is not None:
+            ev[1].record(self.stream)
+
+    def time(self, steps, warmup, world=1):
+        for i in range(warmup):
+            self.run(self.pools[i % 3])
+        torch.cuda.synchronize()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(steps)]
+        pev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(steps)]
+        barrier(world)
+        torch.cuda.synchronize()
+        t0 = time.time()
+        for i in range(steps):
+            self.flush.zero_()  # outside the timed events: write > L2 between steps
+            evs[i][0].record(self.stream)
+            self.run(self.pools[i % 3], ev=pev[i])
+            evs[i][1].record(self.stream)
+        torch.cuda.synchronize()
+        t1 = time.time()
+        barrier(world)
+        if self.pa.get_device_error() != 0:
+            raise RuntimeError("device error word set after the timed region")
+        step_ms = sum(a.elapsed_time(b) for a, b in evs) / steps
+        pre_ms = sum(a.elapsed_time(b) for a, b in pev) / steps
+        return step_ms, pre_ms, t0, t1
+
+    def config(self):
+        w, m = self.w, self.m
+        return {"workload": self.name, "batch": w["batch"], "num_heads": w["num_heads"],
+                "num_kv_heads": w["num_kv_heads"], "head_dim": w["head_dim"],
+                "block_size": w["block_size"], "q_lens": m["q_lens"], "cached": m["cached"],
+                "total_q": self.total_q, "flops_per_step": self.flops,
+                "step": "store_kv(new tokens) + prefill_varlen",
+                "l2": "256 MB buffer written between timed steps (outside the events)"}
+
+    def free(self):
+        del self.pools, self.out, self.flush
+        torch.cuda.empty_cache()
+
+
+def prefill_entry(pa, name, dev, args):
+    b = PrefillBench(pa, name, dev)
+    steps = max(args.steps, 50)
+    step_ms, pre_ms, t0, t1 = b.time(steps, max(3, args.warmup))
+    peak, kind = tensor_peak()
+    achieved = b.flops / (pre_ms / 1e3) / 1e12
+    entry = {
+        "kind": "prefill", "steps": steps, "us_per_step": step_ms * 1e3,
+        "prefill_us": pre_ms * 1e3, "tflops": b.flops / (step_ms / 1e3) / 1e12,
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "peak_kind": f"of {kind} (bf16 dense, burst)",
+                     "kernel": "prefill_kernel (CUDA events per call)"},
+        "gpu_launches": 2 * steps,
+        "config": b.config(),
+        "_wall": (t0, t1),
+    }
+    b.free()
+    if not args.no_cpu_baseline:
+        entry["cpu_baseline"] = cpu_prefill_baseline(name, budget_s=4.0)
+    return entry
 
 
 def run_prefill(args, world, rank, local):
@@ -566,60 +862,20 @@ def run_prefill(args, world, rank, local):
     if rank == 0 or world == 1:
         pabuild.build()
     barrier(world)
-    name = args.workload
-    w = W.WORKLOADS[name]
     dev = torch.device("cuda", torch.cuda.current_device())
-    pools = [W.make_workload(name, device=dev, variant=v + 97 * rank) for v in range(3)]
-    m = pools[0].meta
-    flops = prefill_flops(m["cached"], m["q_lens"], w["num_heads"], w["head_dim"])
-    max_q = max(m["q_lens"])
-    total_q = sum(m["q_lens"])
-    out = torch.empty((total_q, w["num_heads"], w["head_dim"]), dtype=torch.bfloat16, device=dev)
-    # L2 flush buffer: the K/V of one step (~52 MB) fits in L2, so flush between steps
-    flush = torch.empty(256 * 2 ** 20, dtype=torch.uint8, device=dev)
-    stream = torch.cuda.current_stream()
-
-    def step(p):
-        pa.store_kv(p.k_new, p.v_new, p.slot_mapping, p.k_cache, p.v_cache)
-        pa.prefill_varlen(p.q, p.k_cache, p.v_cache, p.block_tables, p.cu_seqlens_q,
-                          p.cu_seqlens_k, p.scale, max_q_len=max_q, out=out)
-
-    for i in range(args.warmup):
-        step(pools[i % 3])
-    torch.cuda.synchronize()
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(args.steps)]
-    pev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(args.steps)]
     sampler = ClockSampler(local) if rank == 0 else None
     if sampler:
         time.sleep(0.3)
-    barrier(world)
-    torch.cuda.synchronize()
-    t_wall0 = time.time()
-    for i in range(args.steps):
-        flush.zero_()  # outside the timed events: write > L2 between steps
-        p = pools[i % 3]
-        evs[i][0].record(stream)
-        pa.store_kv(p.k_new, p.v_new, p.slot_mapping, p.k_cache, p.v_cache)
-        pev[i][0].record(stream)
-        pa.prefill_varlen(p.q, p.k_cache, p.v_cache, p.block_tables, p.cu_seqlens_q,
-                          p.cu_seqlens_k, p.scale, max_q_len=max_q, out=out)
-        pev[i][1].record(stream)
-        evs[i][1].record(stream)
-    torch.cuda.synchronize()
-    t_wall1 = time.time()
-    barrier(world)
+    b = PrefillBench(pa, args.workload, dev, rank=rank)
+    step_ms, pre_ms, t_wall0, t_wall1 = b.time(args.steps, args.warmup, world)
+    step_ms = max_over_ranks(world, step_ms)
+    pre_ms = max_over_ranks(world, pre_ms)
+    total_flops = sum_over_ranks(world, float(b.flops))
+    flops, config = b.flops, b.config()
+    b.free()
     if sampler:
         time.sleep(0.3)
         sampler.stop()
-    if pa.get_device_error() != 0:
-        raise RuntimeError("device error word set after the timed region")
-    step_ms = sum(a.elapsed_time(b) for a, b in evs) / args.steps
-    pre_ms = sum(a.elapsed_time(b) for a, b in pev) / args.steps
-    step_ms = max_over_ranks(world, step_ms)
-    pre_ms = max_over_ranks(world, pre_ms)
-    total_flops = sum_over_ranks(world, float(flops))
     if rank != 0:
         return
     peak, kind = tensor_peak()
@@ -629,13 +885,7 @@ def run_prefill(args, world, rank, local):
             total_flops / (step_ms / 1e3) / 1e12, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic",
-        "config": {"workload": name, "batch": w["batch"], "num_heads": w["num_heads"],
-                   "num_kv_heads": w["num_kv_heads"], "head_dim": w["head_dim"],
-                   "block_size": w["block_size"], "q_lens": m["q_lens"], "cached": m["cached"],
-                   "total_q": total_q, "flops_per_step": flops,
-                   "step": "store_kv(new tokens) + prefill_varlen",
-                   "l2": "256 MB buffer written between timed steps (outside the events)"},
+        "data": "synthetic", "config": config,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": None,
                      "kernel": "prefill_kernel (CUDA events per call)",
@@ -643,6 +893,8 @@ def run_prefill(args, world, rank, local):
         "gpu_launches": 2 * args.steps,
         "clocks": sampler.summary(t_wall0, t_wall1) if sampler else None,
     }
+    if not args.no_cpu_baseline and world == 1:
+        line["cpu_baseline"] = cpu_prefill_baseline(args.workload)
     print(json.dumps(line), flush=True)
 
 
@@ -654,6 +906,8 @@ def main():
     ap.add_argument("--impl", choices=["gpu", "reference"], default="gpu")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(W.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--headline-only", action="store_true",
+                    help="skip the other workloads measured beside the headline decode")
     ap.add_argument("--window", type=int, default=0,
                     help="sliding window in keys (pa_decode_window); 0 = all keys")
     ap.add_argument("--sinks", type=int, default=0, help="leading keys kept with --window")
@@ -666,8 +920,7 @@ def main():
     try:
         if W.WORKLOADS[args.workload]["kind"] == "prefill":
             if args.impl == "reference":
-                print(json.dumps({"impl": "reference", "unavailable":
-                                  "the reference arm times the decode workloads only"}))
+                run_reference_prefill(args, world, rank)
             else:
                 run_prefill(args, world, rank, local)
         elif args.impl == "reference":

@@ -148,6 +148,13 @@ size_t pa_decode_workspace_size(const pa_kv_cache* cache, int32_t batch, int32_t
  *   workspace       device scratch of at least pa_decode_workspace_size()
  *                   bytes (may be NULL when that is 0). Contents on entry are
  *                   ignored; calls sharing one workspace must not overlap.
+ *                   The split-K arrival counters in it carry a per-call tag
+ *                   and each is cleared by its last arrival, so a CUDA graph
+ *                   that captured the call can be replayed back to back on
+ *                   the same workspace (its tag is frozen at capture). After
+ *                   a launch that reported PA_DEVERR_WAIT_TIMEOUT, counters
+ *                   of unfinished segments stay set: make one uncaptured call
+ *                   on the workspace before replaying such a graph again.
  * Arithmetic: bf16 (or E4M3 / INT8 codes widened exactly to f16) operands, fp32 scores,
  * softmax and accumulation, one round to bf16 at the output.
  */
@@ -260,6 +267,24 @@ pa_status pa_decode_noalloc(const void* q, const pa_kv_cache* cache, const int32
  * (PA_DEVERR_* bits, 0 if none) in *code and clear it.
  */
 pa_status pa_get_device_error(uint32_t* code);
+
+/*
+ * pa_debug_inject_wait_timeout - test hook for the failure-detection path; the
+ * pages have no counterpart. Every wait of a decode kernel on a copy is
+ * bounded (2 s by default); after the bound it records PA_DEVERR_WAIT_TIMEOUT,
+ * lets the copies it has in flight land (each wait bounded again) and returns,
+ * so the context stays usable. This hook makes that happen on purpose without
+ * faulting anything: while armed (skip_copy >= 0), decode launches of this
+ * process (persistent kernel, batch <= 2048; pa_decode, pa_decode_window,
+ * pa_decode_append) wait at most wait_limit_ns (1 .. 2e9) per copy, and in
+ * each launch the first warp of the first CTA never issues its skip_copy-th
+ * block copy (counted from 0 in its own block order), so its wait for that
+ * block runs out. Outputs of such a launch are invalid. skip_copy < 0
+ * disarms the hook and restores the 2 s bound (wait_limit_ns ignored).
+ * Process-wide, not thread-safe against concurrent decode calls: arm, run
+ * one call, disarm. Returns PA_ERR_SHAPE for a bound outside 1 .. 2e9.
+ */
+pa_status pa_debug_inject_wait_timeout(int32_t skip_copy, uint64_t wait_limit_ns);
 
 #ifdef __cplusplus
 }

@@ -6,8 +6,9 @@ step of the computation runs in the library's CUDA kernels; this module never
 computes attention itself and has no fallback. If libpa_gb300.so is missing,
 every call raises (build it with ``python -m paged_kv_cache_186_gb300.build``).
 
-Names follow the C ABI: store_kv, decode, decode_workspace_size, prefill_varlen,
-decode_noalloc, get_device_error.
+Names follow the C ABI: store_kv, decode, decode_window, decode_append,
+decode_workspace_size, prefill_varlen, decode_noalloc, get_device_error,
+debug_inject_wait_timeout.
 """
 from __future__ import annotations
 
@@ -37,7 +38,7 @@ DECODE_NOALLOC_SCRATCH_BYTES = 32 << 20
 # Every symbol include/pa.h declares.
 EXPORTED = ("pa_abi_version", "pa_status_string", "pa_store_kv", "pa_decode_workspace_size",
             "pa_decode", "pa_decode_window", "pa_decode_append", "pa_prefill_varlen",
-            "pa_decode_noalloc", "pa_get_device_error")
+            "pa_decode_noalloc", "pa_get_device_error", "pa_debug_inject_wait_timeout")
 
 
 class PAError(RuntimeError):
@@ -93,6 +94,8 @@ def lib() -> ctypes.CDLL:
                                     ctypes.c_float, P, P]
     L.pa_get_device_error.restype = ctypes.c_int
     L.pa_get_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
+    L.pa_debug_inject_wait_timeout.restype = ctypes.c_int
+    L.pa_debug_inject_wait_timeout.argtypes = [i32, ctypes.c_uint64]
     del i64
     _lib = L
     return L
@@ -263,6 +266,13 @@ def decode_noalloc(q, k_cache, v_cache, block_tables, context_lens, scale: float
                                    bt.shape[1], _ptr(cl), int(max_context_len), B, H,
                                    float(scale), _ptr(out), _stream()), "pa_decode_noalloc")
     return out
+
+
+def debug_inject_wait_timeout(skip_copy: int, wait_limit_ns: int = 0) -> None:
+    """pa_debug_inject_wait_timeout: arm (skip_copy >= 0) or disarm (< 0) the
+    failure-detection test hook of the decode kernels."""
+    _check(lib().pa_debug_inject_wait_timeout(int(skip_copy), int(wait_limit_ns)),
+           "pa_debug_inject_wait_timeout")
 
 
 def get_device_error() -> int:

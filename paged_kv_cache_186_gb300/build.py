@@ -55,8 +55,6 @@ def build(force: bool = False, verbose_ptxas: bool = False, jobs: int | None = N
                      "-I", CSRC, "-diag-suppress", "177"]
     if verbose_ptxas:
         common += ["-Xptxas", "-v"]
-    # tuning hook: extra -D defines (e.g. PA_DECODE_STAGE_KB) for kernel sweeps
-    common += os.environ.get("PA_EXTRA_NVCC_FLAGS", "").split()
 
     def compile_one(src: str) -> str:
         obj = os.path.join(BUILD, os.path.basename(src) + ".o")

@@ -10,6 +10,7 @@
 #include <mutex>
 
 #include "pa.h"
+#include "pa_device.cuh"
 #include "pa_launch.h"
 #include "pa_prefill.h"
 
@@ -144,6 +145,12 @@ pa_status cached_cache_map(CUtensorMap* out, void* base, const pa_kv_cache* c) {
   *out = e.map;
   return PA_OK;
 }
+
+// Failure-detection test hook (pa_debug_inject_wait_timeout): the copy the
+// first warp of decode CTA 0 leaves unissued (-1: none) and the wait bound
+// of decode launches (0: kWaitLimitNs).
+std::atomic<int> g_debug_skip_copy{-1};
+std::atomic<unsigned long long> g_debug_wait_limit_ns{0};
 
 // Tag of one decode call in the workspace's arrival counters: increasing,
 // never 0 (a zeroed counter never matches the current call).
@@ -332,6 +339,9 @@ pa_status decode_common(const void* q, const pa_kv_cache* cache, const int32_t* 
   a.num_splits = plan.num_splits;
   a.kv = static_cast<int>(cache->dtype);
   a.scale_log2 = scale * 1.4426950408889634f;  // log2(e): scores kept in base-2 units
+  const unsigned long long limit = g_debug_wait_limit_ns.load();
+  a.wait_limit_ns = limit > 0 ? limit : pa::kWaitLimitNs;
+  a.debug_skip_copy = g_debug_skip_copy.load();
   return pa::launch_decode(a, kmap, vmap, strm) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
@@ -440,6 +450,18 @@ pa_status pa_prefill_varlen(const void* q, const pa_kv_cache* cache, const int32
   return pa::launch_prefill(a, qmap, kmap, vmap, static_cast<cudaStream_t>(stream)) == cudaSuccess
              ? PA_OK
              : PA_ERR_CUDA;
+}
+
+pa_status pa_debug_inject_wait_timeout(int32_t skip_copy, uint64_t wait_limit_ns) {
+  if (skip_copy < 0) {
+    g_debug_skip_copy.store(-1);
+    g_debug_wait_limit_ns.store(0);
+    return PA_OK;
+  }
+  if (wait_limit_ns == 0 || wait_limit_ns > pa::kWaitLimitNs) return PA_ERR_SHAPE;
+  g_debug_wait_limit_ns.store(wait_limit_ns);
+  g_debug_skip_copy.store(skip_copy);
+  return PA_OK;
 }
 
 pa_status pa_get_device_error(uint32_t* code) {

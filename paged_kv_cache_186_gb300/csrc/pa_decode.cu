@@ -36,7 +36,6 @@
 //   * Batches above kMaxPersistentBatch use a grid of (kv head, sequence,
 //     split) CTAs instead, with the same per-block code.
 #include <algorithm>
-#include <cstdlib>
 
 #include "pa_device.cuh"
 #include "pa_launch.h"
@@ -553,7 +552,8 @@ __device__ __forceinline__ SegParts seg_parts(const int* prefix, int B, int Hkv,
 // this call. Every counter is tagged early in the call (tag_counters), so an
 // arrival is normally one atomic add. An add that still finds another call's
 // epoch tags the word itself with a compare-and-swap (whoever tags first wins;
-// nothing resets a tagged word) and counts itself again.
+// only the segment's last arrival clears a tagged word) and counts itself
+// again.
 __device__ __forceinline__ uint32_t tagged_fetch_add(unsigned long long* counter, uint32_t epoch,
                                                      uint32_t* err) {
   const unsigned long long old = atomicAdd(counter, 1ull);
@@ -593,10 +593,18 @@ __device__ __forceinline__ void tag_counters(unsigned long long* counters, long 
   }
 }
 
-// Count this warp's arrival at a segment of `parts` pieces; true for the last.
+// Count this warp's arrival at a segment of `parts` pieces; true for the
+// last. The last arriver also clears the counter (tag 0 is no call's epoch):
+// every other arrival of this call has been counted, so nothing else of this
+// call still needs it, and a launch that repeats this call's epoch (a CUDA
+// graph replays its captured parameters) finds it untagged and starts the
+// count afresh. (A tagging lane of this call that comes later leaves
+// (epoch, 0), which is also a correct starting state.)
 __device__ __forceinline__ bool arrive_last(unsigned long long* counter, uint32_t epoch,
                                             uint32_t parts, uint32_t* err) {
-  return tagged_fetch_add(counter, epoch, err) + 1u == parts;
+  const bool last = tagged_fetch_add(counter, epoch, err) + 1u == parts;
+  if (last) atomicExch(counter, 0ull);
+  return last;
 }
 
 // Merge partials of segment (b, kvh): M = max m_j, l = sum l_j 2^(m_j - M),
@@ -914,6 +922,9 @@ __global__ void __launch_bounds__(NW * 32, 3)
 
   long long win_base = 0;
   int issued = 0;
+  // test hook (off: -1): this warp leaves one copy unissued, so that its
+  // bounded wait for the block runs out; nothing is in flight on that stage
+  const int skip_copy = (blockIdx.x == 0 && warp == 0) ? a.debug_skip_copy : -1;
   auto issue_pending = [&]() {
     if (issued >= nmine) return;
     if (issued - win_base == 32) {
@@ -929,7 +940,7 @@ __global__ void __launch_bounds__(NW * 32, 3)
       if (lane == 0) report_error(a.err, PA_DEVERR_BLOCK_RANGE);
       phys = 0;  // stay inside the pool; the result is flagged as invalid
     }
-    if (lane == 0) {
+    if (lane == 0 && issued != skip_copy) {
       const int s = issued % ST;
       const uint32_t bar = bar0 + 8 * s;
       const uint32_t kt = stage0 + s * C::kStage;
@@ -978,7 +989,7 @@ __global__ void __launch_bounds__(NW * 32, 3)
     for (int vb = cp.lo; vb < cp.hi; ++vb) {
       const int blk = sw.logical(vb);  // visible block -> logical block
       const int s = consumed % ST;
-      const bool got = mbar_wait(bar0 + 8 * s, (consumed / ST) & 1);
+      const bool got = mbar_wait(bar0 + 8 * s, (consumed / ST) & 1, a.wait_limit_ns);
       if (!__all_sync(kFull, got)) {
         ok = false;
         if (lane == 0) report_error(a.err, PA_DEVERR_WAIT_TIMEOUT);
@@ -1023,7 +1034,8 @@ __global__ void __launch_bounds__(NW * 32, 3)
   }
   if (!ok) {
     // give copies still in flight a bounded chance to land before exit
-    for (int i = consumed; i < issued; ++i) (void)mbar_wait(bar0 + 8 * (i % ST), (i / ST) & 1);
+    for (int i = consumed; i < issued; ++i)
+      (void)mbar_wait(bar0 + 8 * (i % ST), (i / ST) & 1, a.wait_limit_ns);
   }
 }
 
@@ -1114,7 +1126,7 @@ __global__ void __launch_bounds__(NW * 32)
   int consumed = 0;
   for (int i = 0; i < n_my; ++i) {
     const int s = i % ST;
-    const bool got = mbar_wait(bar0 + 8 * s, (i / ST) & 1);
+    const bool got = mbar_wait(bar0 + 8 * s, (i / ST) & 1, a.wait_limit_ns);
     if (!__all_sync(kFull, got)) {
       ok = false;
       break;
@@ -1131,7 +1143,7 @@ __global__ void __launch_bounds__(NW * 32)
   if (!ok) {
     if (lane == 0) report_error(a.err, PA_DEVERR_WAIT_TIMEOUT);
     for (int i = consumed; i < min(n_my, consumed + ST); ++i)
-      (void)mbar_wait(bar0 + 8 * (i % ST), (i / ST) & 1);
+      (void)mbar_wait(bar0 + 8 * (i % ST), (i / ST) & 1, a.wait_limit_ns);
   }
   store_warp_state<D, NW, Q8>(merge_buf, warp, lane, m_run, l_run, acc);
   const bool any_fail = __syncthreads_or(!ok);
@@ -1183,16 +1195,10 @@ __global__ void __launch_bounds__(128) decode_split_merge_kernel(const DecodeArg
 }
 
 // ============================================================ host side
-#ifndef PA_DECODE_WARPS
-#define PA_DECODE_WARPS 4
-#endif
-#ifndef PA_DECODE_STAGE_KB
-#define PA_DECODE_STAGE_KB 64
-#endif
-constexpr int kWarps = PA_DECODE_WARPS;
+constexpr int kWarps = 4;
 // Shared-memory budget of one CTA's stage rings (the CTA count per SM follows
 // from it); each warp gets kStageBudget / (kWarps * stage) stages, 2 to 8.
-constexpr int kStageBudget = PA_DECODE_STAGE_KB * 1024;
+constexpr int kStageBudget = 64 * 1024;
 
 constexpr int stages_for(int stage_bytes) {
   return kStageBudget / (kWarps * stage_bytes) < 2 ? 2
@@ -1286,14 +1292,8 @@ struct Inst {
   }
 };
 
-int split_tokens_target() {
-  static int v = [] {
-    const char* s = std::getenv("PA_DECODE_SPLIT_TOKENS");
-    const int x = s ? std::atoi(s) : 0;
-    return x > 0 ? x : 512;
-  }();
-  return v;
-}
+// Tokens per split of the grid-split path.
+constexpr int kSplitTokens = 512;
 
 template <typename F>
 auto dispatch(int head_dim, int block_size, int kv, F&& f)
@@ -1338,7 +1338,7 @@ DecodePlan plan_decode(int batch, int num_heads, int num_kv_heads, int head_dim,
   }
   p.persistent_ctas = 0;
   const int max_nblk = (std::max(len_cap, 0) + block_size - 1) / block_size;
-  int cb = std::max(1, split_tokens_target() / block_size);
+  int cb = std::max(1, kSplitTokens / block_size);
   cb = std::min(cb, 32 * kWarps);  // a warp holds its block ids in one register per lane
   p.blocks_per_split = cb;
   p.num_splits = std::max(1, (max_nblk + cb - 1) / cb);

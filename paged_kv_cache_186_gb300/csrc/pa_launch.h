@@ -73,6 +73,11 @@ struct DecodeArgs {
   int blocks_per_split, num_splits;  // grid-split path
   int kv;                     // kKvBf16, kKvE4m3 or kKvInt8
   float scale_log2;
+  unsigned long long wait_limit_ns;  // bound of every wait on a copy
+  // failure-detection test hook (pa_debug_inject_wait_timeout), -1 when off:
+  // the first warp of CTA 0 never issues its copy number debug_skip_copy, so
+  // its wait for that block runs out
+  int debug_skip_copy;
 };
 
 // Plan of a decode call: persistent (CTA count, 2 partial slots per CTA) or

@@ -44,6 +44,13 @@ def test_abi_version_and_status_strings(L):
     assert L.pa_status_string(99) == b"unknown status"
 
 
+def test_wait_timeout_hook_checks_its_bound(L):
+    # host-only: arming and disarming touch no device
+    assert L.pa_debug_inject_wait_timeout(0, 0) == 2            # PA_ERR_SHAPE
+    assert L.pa_debug_inject_wait_timeout(0, 3_000_000_000) == 2
+    assert L.pa_debug_inject_wait_timeout(-1, 0) == 0           # disarmed
+
+
 def _cache(**kw):
     c = dict(num_blocks=8, block_size=16, num_kv_heads=2, head_dim=64, dtype=pa.PA_KV_BF16,
              k_cache=0x1000, v_cache=0x2000, k_scale=None, v_scale=None)

@@ -321,6 +321,17 @@ def workload_lengths(name: str) -> list[int]:
     return draw_lengths(w["lens"], w["batch"], _gen(w["seed"], "cpu"))
 
 
+def prefill_lengths(name: str) -> tuple[list[int], list[int]]:
+    """(cached lengths, new-token counts) a prefill workload draws (cheap: no tensors)."""
+    w = WORKLOADS[name]
+    g_cpu = _gen(w["seed"], "cpu")
+    cached = torch.randint(w["cached"][0], w["cached"][1] + 1, (w["batch"],),
+                           generator=g_cpu).tolist()
+    qls = torch.randint(w["q_lens"][0], w["q_lens"][1] + 1, (w["batch"],),
+                        generator=g_cpu).tolist()
+    return cached, qls
+
+
 def make_workload(name: str, device="cpu", variant: int = 0):
     """Inputs of one of the named workloads, at full size. `variant` > 0 draws
     another set of values (same lengths and shapes) for rotating buffers."""
@@ -336,10 +347,7 @@ def make_workload(name: str, device="cpu", variant: int = 0):
         return make_decode(w.pop("batch"), w.pop("num_heads"), w.pop("num_kv_heads"),
                            w.pop("head_dim"), w.pop("block_size"), lens,
                            seed=seed + 7 + 7919 * variant, device=device, **w)
-    cached = torch.randint(w["cached"][0], w["cached"][1] + 1, (w["batch"],),
-                           generator=g_cpu).tolist()
-    qls = torch.randint(w["q_lens"][0], w["q_lens"][1] + 1, (w["batch"],),
-                        generator=g_cpu).tolist()
+    cached, qls = prefill_lengths(name)
     return make_prefill(w["batch"], w["num_heads"], w["num_kv_heads"], w["head_dim"],
                         w["block_size"], cached, qls, pool_factor=w["pool_factor"],
                         seed=seed + 7 + 7919 * variant, device=device, scale=w["scale"])
