@@ -74,34 +74,63 @@ __device__ __forceinline__ uint32_t swz(uint32_t tile, int row, int chunk) {
   return tile + sub * (BS * kSwizzleBytes) + row * kSwizzleBytes + ((c ^ (row & 7)) << 4);
 }
 
+// floor(log2 |x|) of a normal float, and 2^k for k in [-126, 127], exactly.
+__device__ __forceinline__ int float_exponent(float x) {
+  return static_cast<int>((__float_as_uint(x) >> 23) & 0xffu) - 127;
+}
+__device__ __forceinline__ float pow2i(int k) {
+  return __uint_as_float(static_cast<uint32_t>(min(max(k, -126), 127) + 127) << 23);
+}
+
 // Q fragments (A operand of S = Q K^T) of kv head `kvh` of sequence b:
 // MMA row r = head r of the group (rows >= G are zero).
 // bf16: k index of step ks = head_dim ks*16 + {2q4, 2q4+1, 2q4+8, 2q4+9}.
 // 8-bit codes (f16 MMA): the head_dim order inside a step is permuted to match how
 // the K codes are read (lane quad q4 owns dims [32 q4, 32 q4 + 32)): step ks
 // uses dims 32 q4 + 4 ks + {0,1} (k = 2q4, 2q4+1) and + {2,3} (k = 2q4+8, +9).
+// The f16 operands of the 8-bit path hold q times a power of two that puts
+// the group's largest |q| in [128, 256): any bf16 q keeps its 8 significant
+// bits (f16 has 11) and cannot overflow f16. q_inv is the inverse factor, to
+// be folded into the score scale (exact: powers of two).
 template <int D, bool Q8>
 __device__ __forceinline__ void load_q(const DecodeArgs& a, int b, int kvh, int lane,
-                                       uint32_t (&qa)[D / 16][2]) {
+                                       uint32_t (&qa)[D / 16][2], float& q_inv) {
   const int G = a.group, r = lane >> 2, q4 = lane & 3;
   const __nv_bfloat16* qrow = static_cast<const __nv_bfloat16*>(a.q) +
                               (static_cast<long long>(b) * a.num_heads + kvh * G + min(r, G - 1)) * D;
+  if constexpr (!Q8) {
 #pragma unroll
-  for (int ks = 0; ks < D / 16; ++ks) {
-    if (r < G) {
-      if constexpr (!Q8) {
+    for (int ks = 0; ks < D / 16; ++ks) {
+      if (r < G) {
         qa[ks][0] = *reinterpret_cast<const uint32_t*>(qrow + ks * 16 + 2 * q4);
         qa[ks][1] = *reinterpret_cast<const uint32_t*>(qrow + ks * 16 + 8 + 2 * q4);
       } else {
-        const uint2 raw4 = *reinterpret_cast<const uint2*>(qrow + 32 * q4 + 4 * ks);
-        const __nv_bfloat162 lo = *reinterpret_cast<const __nv_bfloat162*>(&raw4.x);
-        const __nv_bfloat162 hi = *reinterpret_cast<const __nv_bfloat162*>(&raw4.y);
-        qa[ks][0] = pack_f16x2(__low2float(lo), __high2float(lo));
-        qa[ks][1] = pack_f16x2(__low2float(hi), __high2float(hi));
+        qa[ks][0] = 0u;
+        qa[ks][1] = 0u;
       }
-    } else {
-      qa[ks][0] = 0u;
-      qa[ks][1] = 0u;
+    }
+    q_inv = 1.f;
+  } else {
+    uint2 raw[D / 16];
+    uint32_t amax_bits = 0u;  // largest |q| of the lane, as bits (non-negative floats)
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+      raw[ks] = r < G ? *reinterpret_cast<const uint2*>(qrow + 32 * q4 + 4 * ks) : make_uint2(0u, 0u);
+      // |bf16| pairs as bits: clear the sign bits, then compare the 16-bit halves
+      const uint32_t x = raw[ks].x & 0x7fff7fffu, y = raw[ks].y & 0x7fff7fffu;
+      amax_bits = max(amax_bits, max(max(x >> 16, x & 0xffffu), max(y >> 16, y & 0xffffu)));
+    }
+    amax_bits = __reduce_max_sync(kFull, amax_bits);
+    const float amax = __uint_as_float(amax_bits << 16);  // bf16 bits -> float
+    const int k = amax > 0.f ? 7 - float_exponent(amax) : 0;
+    const float qf = pow2i(k);
+    q_inv = pow2i(-k);
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+      const __nv_bfloat162 lo = *reinterpret_cast<const __nv_bfloat162*>(&raw[ks].x);
+      const __nv_bfloat162 hi = *reinterpret_cast<const __nv_bfloat162*>(&raw[ks].y);
+      qa[ks][0] = pack_f16x2(__low2float(lo) * qf, __high2float(lo) * qf);
+      qa[ks][1] = pack_f16x2(__low2float(hi) * qf, __high2float(hi) * qf);
     }
   }
 }
@@ -118,7 +147,7 @@ __device__ __forceinline__ void attend_block(uint32_t kt, uint32_t vt, const uin
                                              int tok0, int L, int hole_lo, int hole_hi,
                                              const uint32_t (&qa)[D / 16][2],
                                              float (&acc)[D / 16][4], float& m_run, float& l_run,
-                                             float sl2, int lane) {
+                                             float& vfac, float sl2, int lane) {
   constexpr int NT = BS / 8;  // n-tiles of 8 tokens
   constexpr int NG = BS / 16;  // 16-token groups (k-steps of P.V)
   constexpr bool Q8 = KV != kKvBf16;
@@ -211,6 +240,48 @@ __device__ __forceinline__ void attend_block(uint32_t kt, uint32_t vt, const uin
   }
   l_run += psum;
   m_run = m_new;
+  // ---- 8-bit V: the f16 operand P' = p * v_scale * vfac. vfac is a power of
+  // two chosen so that the block's largest V scale times vfac lies in
+  // [2^-4, 2^12] (P' <= 4096 since p <= 1: no f16 overflow, and no f16
+  // subnormals for any p above 2^-10); when a block falls outside, vfac moves
+  // to put it at [128, 256) and acc, which holds sum P' v, is rescaled by the
+  // same power of two (exact). The writers divide acc by vfac.
+  float vsf[NG][4];
+  if constexpr (Q8) {
+    float vm = 0.f;
+#pragma unroll
+    for (int hg = 0; hg < NG; ++hg) {
+      const int g0 = tok0 + hg * 16 + 2 * q4;
+      const float2 v0 = *reinterpret_cast<const float2*>(vsc + hg * 16 + 2 * q4);
+      const float2 v1 = *reinterpret_cast<const float2*>(vsc + hg * 16 + 8 + 2 * q4);
+      // masked keys' scales may hold anything: they take no part
+      vsf[hg][0] = valid(g0) ? v0.x : 0.f;
+      vsf[hg][1] = valid(g0 + 1) ? v0.y : 0.f;
+      vsf[hg][2] = valid(g0 + 8) ? v1.x : 0.f;
+      vsf[hg][3] = valid(g0 + 9) ? v1.y : 0.f;
+      vm = fmaxf(vm, fmaxf(fmaxf(vsf[hg][0], vsf[hg][1]), fmaxf(vsf[hg][2], vsf[hg][3])));
+    }
+    // the 4 lanes of a quad cover the block's tokens; every quad holds the same
+    vm = fmaxf(vm, __shfl_xor_sync(kFull, vm, 1));
+    vm = fmaxf(vm, __shfl_xor_sync(kFull, vm, 2));
+    const float t = vm * vfac;
+    if (vm > 0.f && !(t >= 0.0625f && t <= 4096.f)) {  // warp-uniform
+      const float nf = pow2i(7 - float_exponent(vm));
+      const float ratio = nf / vfac;  // a power of two
+#pragma unroll
+      for (int mt = 0; mt < D / 16; ++mt) {
+        acc[mt][0] *= ratio;
+        acc[mt][1] *= ratio;
+        acc[mt][2] *= ratio;
+        acc[mt][3] *= ratio;
+      }
+      vfac = nf;
+    }
+#pragma unroll
+    for (int hg = 0; hg < NG; ++hg)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) vsf[hg][j] *= vfac;
+  }
   // ---- O^T += V^T P^T, one k-step per 16-token group
 #pragma unroll
   for (int hg = 0; hg < NG; ++hg) {
@@ -243,12 +314,9 @@ __device__ __forceinline__ void attend_block(uint32_t kt, uint32_t vt, const uin
         }
       }
     } else {
-      const float2 v0 = *reinterpret_cast<const float2*>(vsc + hg * 16 + 2 * q4);
-      const float2 v1 = *reinterpret_cast<const float2*>(vsc + hg * 16 + 8 + 2 * q4);
-      // masked tokens have p = 0 but their scales may be anything: select, not multiply
-      const uint32_t pb0 = pack_f16x2(valid(g0) ? p0 * v0.x : 0.f, valid(g0 + 1) ? p1 * v0.y : 0.f);
-      const uint32_t pb1 =
-          pack_f16x2(valid(g0 + 8) ? p8 * v1.x : 0.f, valid(g0 + 9) ? p9 * v1.y : 0.f);
+      // masked tokens have p = 0 and a zeroed scale
+      const uint32_t pb0 = pack_f16x2(p0 * vsf[hg][0], p1 * vsf[hg][1]);
+      const uint32_t pb1 = pack_f16x2(p8 * vsf[hg][2], p9 * vsf[hg][3]);
       // lane (r, q4) reads 16-byte chunk r of token rows 2q4, 2q4+1, 2q4+8, 2q4+9:
       // word w gives dims 16r + 4w + {0..3}; output row mapping in the writers.
       const int t0 = hg * 16 + 2 * q4;
@@ -284,7 +352,8 @@ __device__ __forceinline__ void attend_block(uint32_t kt, uint32_t vt, const uin
 // Write a warp's (max, sum, O) for its 8 head rows into the merge buffer.
 template <int D, int NW, bool Q8>
 __device__ __forceinline__ void store_warp_state(float* mo, int warp, int lane, float m_run,
-                                                 float l_run, const float (&acc)[D / 16][4]) {
+                                                 float l_run, float o_scale,
+                                                 const float (&acc)[D / 16][4]) {
   constexpr int S = D + 4;
   const int r = lane >> 2, q4 = lane & 3;
   float l_tot = l_run + __shfl_xor_sync(kFull, l_run, 1);
@@ -307,10 +376,10 @@ __device__ __forceinline__ void store_warp_state(float* mo, int warp, int lane, 
     }
     float* row0 = mo + (warp * 8 + 2 * q4) * S;
     float* row1 = row0 + S;
-    row0[d0] = acc[mt][0];
-    row1[d0] = acc[mt][1];
-    row0[d1] = acc[mt][2];
-    row1[d1] = acc[mt][3];
+    row0[d0] = acc[mt][0] * o_scale;
+    row1[d0] = acc[mt][1] * o_scale;
+    row0[d1] = acc[mt][2] * o_scale;
+    row1[d1] = acc[mt][3] * o_scale;
   }
 }
 
@@ -441,8 +510,8 @@ __device__ __forceinline__ void piece_next(Piece& p, const int* prefix, int B, i
 template <int D, bool Q8>
 __device__ __forceinline__ void write_warp_result(const DecodeArgs& a, int b, int kvh,
                                                   bool final_out, long long slot, int lane,
-                                                  float m_run, float l_run,
-                                                  const float (&acc)[D / 16][4]) {
+                                                  float m_run, float l_run, float o_scale,
+                                                  float (&acc)[D / 16][4]) {
   const int r = lane >> 2, q4 = lane & 3, G = a.group;
   float l_tot = l_run + __shfl_xor_sync(kFull, l_run, 1);
   l_tot += __shfl_xor_sync(kFull, l_tot, 2);
@@ -450,7 +519,7 @@ __device__ __forceinline__ void write_warp_result(const DecodeArgs& a, int b, in
   const float l0 = __shfl_sync(kFull, l_tot, 4 * h0);
   const float l1 = __shfl_sync(kFull, l_tot, 4 * h1);
   if (final_out) {
-    const float inv0 = l0 > 0.f ? 1.f / l0 : 0.f, inv1 = l1 > 0.f ? 1.f / l1 : 0.f;
+    const float inv0 = l0 > 0.f ? o_scale / l0 : 0.f, inv1 = l1 > 0.f ? o_scale / l1 : 0.f;
     __nv_bfloat16* o = static_cast<__nv_bfloat16*>(a.out) +
                        (static_cast<long long>(b) * a.num_heads + kvh * G) * D;
 #pragma unroll
@@ -470,6 +539,12 @@ __device__ __forceinline__ void write_warp_result(const DecodeArgs& a, int b, in
     return;
   }
   float* po = a.part_o + slot * a.slot_rows * D;
+  if constexpr (Q8) {
+#pragma unroll
+    for (int mt = 0; mt < D / 16; ++mt)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) acc[mt][j] *= o_scale;
+  }
 #pragma unroll
   for (int mt = 0; mt < D / 16; ++mt) {
     int d0, d1;
@@ -979,13 +1054,15 @@ __global__ void __launch_bounds__(NW * 32, 3)
   bool ok = true;
   while (ok && cp.valid) {
     uint32_t qa[D / 16][2];
-    load_q<D, Q8>(a, cp.b, cp.kvh, lane, qa);
+    float q_inv;
+    load_q<D, Q8>(a, cp.b, cp.kvh, lane, qa, q_inv);
+    const float sl2p = sl2 * q_inv;
     const int L = min(max(a.context_lens[cp.b], 0), a.len_cap);
     const SeqWindow sw = seq_window<BS>(L, WIN ? a.window : 0, a.sinks);
     float acc[D / 16][4];
 #pragma unroll
     for (int mt = 0; mt < D / 16; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
-    float m_run = -INFINITY, l_run = 0.f;
+    float m_run = -INFINITY, l_run = 0.f, vfac = 1.f;
     for (int vb = cp.lo; vb < cp.hi; ++vb) {
       const int blk = sw.logical(vb);  // visible block -> logical block
       const int s = consumed % ST;
@@ -1003,7 +1080,8 @@ __global__ void __launch_bounds__(NW * 32, 3)
                                a.block_tables + static_cast<long long>(cp.b) * a.max_blocks + blk,
                                cp.b * Hkv + cp.kvh, (L - 1) - blk * BS, a, lane);
       attend_block<D, BS, KV, WIN>(kt, kt + C::kTile, base_ptr, base, ksc, ksc + BS, blk * BS, L,
-                                    sw.hole_lo, sw.hole_hi, qa, acc, m_run, l_run, sl2, lane);
+                                    sw.hole_lo, sw.hole_hi, qa, acc, m_run, l_run, vfac, sl2p,
+                                    lane);
       ++consumed;
       __syncwarp();
       issue_pending();
@@ -1011,7 +1089,7 @@ __global__ void __launch_bounds__(NW * 32, 3)
     if (!ok) break;
     const bool whole = cp.lo == 0 && cp.hi == cp.nblk;
     write_warp_result<D, Q8>(a, cp.b, cp.kvh, whole, 2 * gw + (cp.lo == 0 ? 1 : 0), lane, m_run,
-                              l_run, acc);
+                              l_run, 1.f / vfac, acc);
     if (!whole) {
       // publish the partial, count the arrival; the last warp merges the segment
       __threadfence();
@@ -1116,11 +1194,13 @@ __global__ void __launch_bounds__(NW * 32)
   for (int i = 0; i < n_pre; ++i) issue(i);
 
   uint32_t qa[D / 16][2];
-  load_q<D, Q8>(a, b, kvh, lane, qa);
+  float q_inv;
+  load_q<D, Q8>(a, b, kvh, lane, qa, q_inv);
+  const float sl2p = a.scale_log2 * q_inv;
   float acc[D / 16][4];
 #pragma unroll
   for (int mt = 0; mt < D / 16; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
-  float m_run = -INFINITY, l_run = 0.f;
+  float m_run = -INFINITY, l_run = 0.f, vfac = 1.f;
 
   bool ok = true;
   int consumed = 0;
@@ -1135,8 +1215,8 @@ __global__ void __launch_bounds__(NW * 32)
     const uint32_t kt = stage0 + s * C::kStage;
     const float* ksc = scale_ptr + ((warp * ST + s) * 2) * BS;
     attend_block<D, BS, KV>(kt, kt + C::kTile, base_ptr, base, ksc, ksc + BS,
-                             (blk0 + warp + i * NW) * BS, L, 0, 0, qa, acc, m_run, l_run,
-                             a.scale_log2, lane);
+                             (blk0 + warp + i * NW) * BS, L, 0, 0, qa, acc, m_run, l_run, vfac,
+                             sl2p, lane);
     __syncwarp();
     if (i + ST < n_my) issue(i + ST);
   }
@@ -1145,7 +1225,7 @@ __global__ void __launch_bounds__(NW * 32)
     for (int i = consumed; i < min(n_my, consumed + ST); ++i)
       (void)mbar_wait(bar0 + 8 * (i % ST), (i / ST) & 1, a.wait_limit_ns);
   }
-  store_warp_state<D, NW, Q8>(merge_buf, warp, lane, m_run, l_run, acc);
+  store_warp_state<D, NW, Q8>(merge_buf, warp, lane, m_run, l_run, 1.f / vfac, acc);
   const bool any_fail = __syncthreads_or(!ok);
   if (any_fail) return;
   // partial slot of (b, kvh, split): the merge kernel below reads these
