@@ -93,31 +93,45 @@ __device__ __forceinline__ float pow2i(int k) {
 // bits (f16 has 11) and cannot overflow f16. q_inv is the inverse factor, to
 // be folded into the score scale (exact: powers of two).
 template <int D, bool Q8>
-__device__ __forceinline__ void load_q(const DecodeArgs& a, int b, int kvh, int lane,
-                                       uint32_t (&qa)[D / 16][2], float& q_inv) {
+__device__ __forceinline__ void fetch_q(const DecodeArgs& a, int b, int kvh, int lane,
+                                        uint32_t (&raw)[D / 16][2]) {
   const int G = a.group, r = lane >> 2, q4 = lane & 3;
   const __nv_bfloat16* qrow = static_cast<const __nv_bfloat16*>(a.q) +
                               (static_cast<long long>(b) * a.num_heads + kvh * G + min(r, G - 1)) * D;
+#pragma unroll
+  for (int ks = 0; ks < D / 16; ++ks) {
+    if (r < G) {
+      if constexpr (!Q8) {
+        raw[ks][0] = *reinterpret_cast<const uint32_t*>(qrow + ks * 16 + 2 * q4);
+        raw[ks][1] = *reinterpret_cast<const uint32_t*>(qrow + ks * 16 + 8 + 2 * q4);
+      } else {
+        const uint2 v = *reinterpret_cast<const uint2*>(qrow + 32 * q4 + 4 * ks);
+        raw[ks][0] = v.x;
+        raw[ks][1] = v.y;
+      }
+    } else {
+      raw[ks][0] = 0u;
+      raw[ks][1] = 0u;
+    }
+  }
+}
+
+template <int D, bool Q8>
+__device__ __forceinline__ void finish_q(const uint32_t (&raw)[D / 16][2],
+                                         uint32_t (&qa)[D / 16][2], float& q_inv) {
   if constexpr (!Q8) {
 #pragma unroll
     for (int ks = 0; ks < D / 16; ++ks) {
-      if (r < G) {
-        qa[ks][0] = *reinterpret_cast<const uint32_t*>(qrow + ks * 16 + 2 * q4);
-        qa[ks][1] = *reinterpret_cast<const uint32_t*>(qrow + ks * 16 + 8 + 2 * q4);
-      } else {
-        qa[ks][0] = 0u;
-        qa[ks][1] = 0u;
-      }
+      qa[ks][0] = raw[ks][0];
+      qa[ks][1] = raw[ks][1];
     }
     q_inv = 1.f;
   } else {
-    uint2 raw[D / 16];
     uint32_t amax_bits = 0u;  // largest |q| of the lane, as bits (non-negative floats)
 #pragma unroll
     for (int ks = 0; ks < D / 16; ++ks) {
-      raw[ks] = r < G ? *reinterpret_cast<const uint2*>(qrow + 32 * q4 + 4 * ks) : make_uint2(0u, 0u);
       // |bf16| pairs as bits: clear the sign bits, then compare the 16-bit halves
-      const uint32_t x = raw[ks].x & 0x7fff7fffu, y = raw[ks].y & 0x7fff7fffu;
+      const uint32_t x = raw[ks][0] & 0x7fff7fffu, y = raw[ks][1] & 0x7fff7fffu;
       amax_bits = max(amax_bits, max(max(x >> 16, x & 0xffffu), max(y >> 16, y & 0xffffu)));
     }
     amax_bits = __reduce_max_sync(kFull, amax_bits);
@@ -127,12 +141,20 @@ __device__ __forceinline__ void load_q(const DecodeArgs& a, int b, int kvh, int 
     q_inv = pow2i(-k);
 #pragma unroll
     for (int ks = 0; ks < D / 16; ++ks) {
-      const __nv_bfloat162 lo = *reinterpret_cast<const __nv_bfloat162*>(&raw[ks].x);
-      const __nv_bfloat162 hi = *reinterpret_cast<const __nv_bfloat162*>(&raw[ks].y);
+      const __nv_bfloat162 lo = *reinterpret_cast<const __nv_bfloat162*>(&raw[ks][0]);
+      const __nv_bfloat162 hi = *reinterpret_cast<const __nv_bfloat162*>(&raw[ks][1]);
       qa[ks][0] = pack_f16x2(__low2float(lo) * qf, __high2float(lo) * qf);
       qa[ks][1] = pack_f16x2(__low2float(hi) * qf, __high2float(hi) * qf);
     }
   }
+}
+
+template <int D, bool Q8>
+__device__ __forceinline__ void load_q(const DecodeArgs& a, int b, int kvh, int lane,
+                                       uint32_t (&qa)[D / 16][2], float& q_inv) {
+  uint32_t raw[D / 16][2];
+  fetch_q<D, Q8>(a, b, kvh, lane, raw);
+  finish_q<D, Q8>(raw, qa, q_inv);
 }
 
 // One physical block (tokens tok0 .. tok0+BS-1, of which those < L count)
@@ -685,33 +707,39 @@ __device__ __forceinline__ bool arrive_last(unsigned long long* counter, uint32_
 // Merge partials of segment (b, kvh): M = max m_j, l = sum l_j 2^(m_j - M),
 // o = sum o_j 2^(m_j - M) (scores in base 2), for all G heads at once. With
 // `final_out` the bf16 rows o / l are written; otherwise (M, l, o) is stored
-// as one partial in the slot of the list's first part. Lane = (part j, head
-// g) with GP lanes per part (G rounded up to a power of two): one round of
-// loads gives every (max, sum), combined online within a lane and across
-// lanes by shuffles; then each lane accumulates D/32 dims of every head over
-// the parts with independent loads. Partials are read through L2.
+// as one partial in the slot of the list's first part. Lane = (head g, slice
+// sub of head_dim) with LPH lanes per head (32 / GP, GP = G rounded up to a
+// power of two, at most head_dim / 8). The lanes of a head first combine the (max, sum) of the
+// parts among themselves (a quarter, an eighth ... of the parts each, then
+// shuffles); then every part costs one round of independent loads (its max
+// and the lane's head_dim slice of O), two parts in flight at a time.
+// Partials are read through L2.
 template <int D, int GP>
 __device__ __forceinline__ void merge_segment_g(const DecodeArgs& a, const PartList& sp, int b,
                                                 int kvh, bool final_out, int lane) {
-  constexpr int V = D / 32;
-  constexpr int PR = 32 / GP;  // parts per round
+  // lanes per head (at least 8 dims each, so a slice is whole 16-byte bf16 stores)
+  constexpr int LPH = (32 / GP) < (D / 8) ? (32 / GP) : (D / 8);
+  constexpr int DL = D / LPH;    // head_dim slice of a lane
+  constexpr int V4 = DL / 4;     // float4 of it
+  static_assert(DL % 8 == 0 && LPH * GP <= 32, "slices of whole 16-byte stores");
   const int G = a.group;
-  const int j_l = lane / GP, g_l = lane % GP;
-  const bool g_ok = g_l < G;
-  // ---- (max, sum) per head, online over rounds and lanes
+  const int g = lane / LPH, sub = lane % LPH;
+  const bool g_ok = g < G;
+  // ---- (max, sum) of head g, online over this lane's parts, then the head's lanes
   float M = -INFINITY, L = 0.f;
-  for (int j0 = 0; j0 < sp.n; j0 += PR) {
-    const int j = j0 + j_l;
-    if (j < sp.n && g_ok) {
+  if (g_ok) {
+    for (int j = sub; j < sp.n; j += LPH) {
       const float2 ml =
-          __ldcg(reinterpret_cast<const float2*>(a.part_ml + (sp.slot(j) * GP + g_l) * 2));
+          __ldcg(reinterpret_cast<const float2*>(a.part_ml + (sp.slot(j) * GP + g) * 2));
       const float m2 = fmaxf(M, ml.x);
-      L = L * fast_exp2(M - m2) + ml.y * fast_exp2(ml.x - m2);
-      M = m2;
+      if (m2 != -INFINITY) {
+        L = L * fast_exp2(M - m2) + ml.y * fast_exp2(ml.x - m2);
+        M = m2;
+      }
     }
   }
 #pragma unroll
-  for (int o = 16; o >= GP; o >>= 1) {
+  for (int o = LPH / 2; o >= 1; o >>= 1) {
     const float Mo = __shfl_xor_sync(kFull, M, o), Lo = __shfl_xor_sync(kFull, L, o);
     const float m2 = fmaxf(M, Mo);
     if (m2 != -INFINITY) {
@@ -719,63 +747,52 @@ __device__ __forceinline__ void merge_segment_g(const DecodeArgs& a, const PartL
       M = m2;
     }
   }
-  // ---- outputs: lane holds dims lane*V .. +V-1 of every head
-  float acc[GP][V];
+  // ---- O: the lane's slice of head g, summed over the parts
+  float acc[DL];
 #pragma unroll
-  for (int g = 0; g < GP; ++g)
+  for (int v = 0; v < DL; ++v) acc[v] = 0.f;
+  if (g_ok) {
+#pragma unroll 2
+    for (int j = 0; j < sp.n; ++j) {
+      const long long row = sp.slot(j) * GP + g;
+      const float m = __ldcg(a.part_ml + row * 2);
+      float4 x[V4];
+      const float4* src = reinterpret_cast<const float4*>(a.part_o + row * D + sub * DL);
 #pragma unroll
-    for (int v = 0; v < V; ++v) acc[g][v] = 0.f;
-  for (int j0 = 0; j0 < sp.n; j0 += PR) {
-    float f = 0.f;
-    const int j = j0 + j_l;
-    if (j < sp.n && g_ok) f = fast_exp2(__ldcg(a.part_ml + (sp.slot(j) * GP + g_l) * 2) - M);
+      for (int v = 0; v < V4; ++v) x[v] = __ldcg(src + v);
+      const float f = m == -INFINITY ? 0.f : fast_exp2(m - M);
 #pragma unroll
-    for (int jj = 0; jj < PR; ++jj) {
-#pragma unroll
-      for (int g = 0; g < GP; ++g) {
-        const float fv = __shfl_sync(kFull, f, jj * GP + g);
-        if (j0 + jj < sp.n && g < G) {
-          const float* src = a.part_o + (sp.slot(j0 + jj) * GP + g) * D + lane * V;
-          if constexpr (V == 4) {
-            const float4 x = __ldcg(reinterpret_cast<const float4*>(src));
-            acc[g][0] += fv * x.x; acc[g][1] += fv * x.y; acc[g][2] += fv * x.z; acc[g][3] += fv * x.w;
-          } else {
-            const float2 x = __ldcg(reinterpret_cast<const float2*>(src));
-            acc[g][0] += fv * x.x; acc[g][1] += fv * x.y;
-          }
-        }
+      for (int v = 0; v < V4; ++v) {
+        acc[4 * v + 0] += f * x[v].x;
+        acc[4 * v + 1] += f * x[v].y;
+        acc[4 * v + 2] += f * x[v].z;
+        acc[4 * v + 3] += f * x[v].w;
       }
     }
   }
+  __syncwarp();  // every lane has read the first part's slot before it is overwritten
+  if (!g_ok) return;
   if (!final_out) {
     // one partial of the merged parts, in the slot of the first of them
-    const long long slot = sp.slot(0);
-    if (j_l == 0 && g_ok) {
-      a.part_ml[(slot * GP + g_l) * 2 + 0] = M;
-      a.part_ml[(slot * GP + g_l) * 2 + 1] = L;
-    }
+    const long long row = sp.slot(0) * GP + g;
+    if (sub == 0) *reinterpret_cast<float2*>(a.part_ml + row * 2) = make_float2(M, L);
+    float4* dst = reinterpret_cast<float4*>(a.part_o + row * D + sub * DL);
 #pragma unroll
-    for (int g = 0; g < GP; ++g) {
-      if (g < G) {
-        float* dst = a.part_o + (slot * GP + g) * D + lane * V;
-#pragma unroll
-        for (int v = 0; v < V; ++v) dst[v] = acc[g][v];
-      }
-    }
+    for (int v = 0; v < V4; ++v)
+      dst[v] = make_float4(acc[4 * v], acc[4 * v + 1], acc[4 * v + 2], acc[4 * v + 3]);
     return;
   }
+  const float inv = L > 0.f ? 1.f / L : 0.f;
+  __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.out) +
+                       (static_cast<long long>(b) * a.num_heads + kvh * G + g) * D + sub * DL;
 #pragma unroll
-  for (int g = 0; g < GP; ++g) {
-    const float lg = __shfl_sync(kFull, L, g);
-    if (g < G) {
-      const float inv = lg > 0.f ? 1.f / lg : 0.f;
-      __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.out) +
-                           (static_cast<long long>(b) * a.num_heads + kvh * G + g) * D + lane * V;
-#pragma unroll
-      for (int v = 0; v < V; v += 2)
-        *reinterpret_cast<__nv_bfloat162*>(dst + v) =
-            __floats2bfloat162_rn(acc[g][v] * inv, acc[g][v + 1] * inv);
-    }
+  for (int v = 0; v < DL; v += 8) {
+    uint4 w;
+    w.x = pack_bf16x2(acc[v] * inv, acc[v + 1] * inv);
+    w.y = pack_bf16x2(acc[v + 2] * inv, acc[v + 3] * inv);
+    w.z = pack_bf16x2(acc[v + 4] * inv, acc[v + 5] * inv);
+    w.w = pack_bf16x2(acc[v + 6] * inv, acc[v + 7] * inv);
+    *reinterpret_cast<uint4*>(dst + v) = w;
   }
 }
 
@@ -984,14 +1001,14 @@ __global__ void __launch_bounds__(NW * 32, 3)
 
   // ---- from here on: memory the previous launch may write
   grid_dependency_wait();
-  if (blockIdx.x == 0) {
-    // sequences without keys: zero output rows (no warp owns any of their blocks)
-    for (int i = threadIdx.x; i < B * a.num_heads * (D / 8); i += NW * 32) {
-      const int row = i / (D / 8), b = row / a.num_heads;
-      if (prefix[b + 1] == prefix[b])
-        reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) +
-                                 static_cast<long long>(row) * D)[i % (D / 8)] = make_uint4(0, 0, 0, 0);
-    }
+  // sequences without keys: zero output rows (no warp owns any of their
+  // blocks). Sequence b is checked by CTA b mod gridDim.x, so no CTA scans
+  // more than ceil(B / gridDim.x) of them.
+  for (int b = blockIdx.x; b < B; b += gridDim.x) {
+    if (prefix[b + 1] != prefix[b]) continue;  // uniform over the CTA
+    uint4* const row = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) +
+                                                static_cast<long long>(b) * a.num_heads * D);
+    for (int i = threadIdx.x; i < a.num_heads * (D / 8); i += NW * 32) row[i] = make_uint4(0, 0, 0, 0);
   }
   if (!active) return;
 
@@ -1037,25 +1054,30 @@ __global__ void __launch_bounds__(NW * 32, 3)
     ++issued;
   };
   for (int s = 0; s < ST; ++s) issue_pending();
-  {
-    // while the first loads are in flight: tag this warp's share of the
-    // segment arrival counters
+  // This warp's share of the segment arrival counters is tagged with the
+  // call's epoch once its first block has been attended to (off the path to
+  // the first block; an arrival that comes earlier tags the word itself).
+  auto tag_my_counters = [&]() {
     const long long nctr = static_cast<long long>(B) * Hkv;
     const long long per = (nctr + W - 1) / W;
     tag_counters(a.seg_counters, gw * per, min(nctr, (gw + 1) * per),
                  may_group ? a.grp_counters + 2 * gw : nullptr, a.epoch, lane);
-  }
+  };
 
-  // ---- consumer: pieces in order
+  // ---- consumer: pieces in order. The next piece's q is fetched before the
+  // current piece's result is written, so its latency overlaps the write,
+  // the arrival and any merge.
   Piece cp;
   piece_first(cp, prefix, B, Hkv, r0, r1);
   const float sl2 = a.scale_log2;
   int consumed = 0;
   bool ok = true;
+  uint32_t qraw[D / 16][2];
+  if (cp.valid) fetch_q<D, Q8>(a, cp.b, cp.kvh, lane, qraw);
   while (ok && cp.valid) {
     uint32_t qa[D / 16][2];
     float q_inv;
-    load_q<D, Q8>(a, cp.b, cp.kvh, lane, qa, q_inv);
+    finish_q<D, Q8>(qraw, qa, q_inv);
     const float sl2p = sl2 * q_inv;
     const int L = min(max(a.context_lens[cp.b], 0), a.len_cap);
     const SeqWindow sw = seq_window<BS>(L, WIN ? a.window : 0, a.sinks);
@@ -1085,8 +1107,12 @@ __global__ void __launch_bounds__(NW * 32, 3)
       ++consumed;
       __syncwarp();
       issue_pending();
+      if (consumed == 1) tag_my_counters();
     }
     if (!ok) break;
+    Piece nx = cp;
+    piece_next(nx, prefix, B, Hkv, r1);
+    if (nx.valid) fetch_q<D, Q8>(a, nx.b, nx.kvh, lane, qraw);
     const bool whole = cp.lo == 0 && cp.hi == cp.nblk;
     write_warp_result<D, Q8>(a, cp.b, cp.kvh, whole, 2 * gw + (cp.lo == 0 ? 1 : 0), lane, m_run,
                               l_run, 1.f / vfac, acc);
@@ -1108,7 +1134,7 @@ __global__ void __launch_bounds__(NW * 32, 3)
         }
       }
     }
-    piece_next(cp, prefix, B, Hkv, r1);
+    cp = nx;
   }
   if (!ok) {
     // give copies still in flight a bounded chance to land before exit
