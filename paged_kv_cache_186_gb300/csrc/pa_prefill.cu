@@ -12,23 +12,27 @@
 //   * A query tile is 128 rows = 128/G tokens x the G query heads of one kv
 //     head (GQA packing: every K/V tile serves the whole head group). One CTA
 //     per SM holds TWO consecutive query tiles of a (sequence, kv head) and
-//     walks the K/V tiles (128 keys) they need.
-//   * Warp 0 streams the two Q tiles once and K/V tiles through a 2-stage ring
-//     (128/bs physical blocks per tile, one 3-D TMA box per block and 64-dim
-//     half, 128B-swizzled), resolving logical -> physical blocks through the
-//     block table; blocks past the last needed key are fetched out of bounds
-//     so TMA fills them with zeros.
-//   * Warp 1 issues the tensor-core MMAs (tcgen05, fp32 accumulation in TMEM)
-//     in the order S0 = Q0 K^T, S1 = Q1 K^T, O0 += P0 V, O1 += P1 V for each
-//     K/V tile: while one softmax warpgroup works on its tile, the tensor core
-//     is busy with the other one's.
-//   * Warps 2-5 (tile 0) and 6-9 (tile 1) own one TMEM lane (= query row)
+//     walks the K/V tiles (128 keys) they need, so every K/V byte brought in
+//     serves 256 query rows.
+//   * Warp 8 streams the two Q tiles once and the K tiles, warp 10 the V
+//     tiles, each through its own 2-stage ring (one 3-D TMA box per physical
+//     block and 64-dim half, 128B-swizzled). Block ids are read 32 at a
+//     time, a window ahead, so no copy waits for a block-table read; blocks
+//     past the last needed key are fetched out of bounds so TMA fills them
+//     with zeros.
+//   * Warp 9 issues the tensor-core MMAs (tcgen05, fp32 accumulation in TMEM)
+//     per key tile n: P_0 V(n), S_0 = Q_0 K(n+1)^T, P_1 V(n), S_1 = Q_1
+//     K(n+1)^T. P_i is stored over S_i, so S_i(n+1) waits for P_i V(n) to
+//     finish; while one tile's softmax runs, the tensor pipe works on the
+//     other's. Its waits suspend in mbarrier try_wait: a spinning warp would
+//     take issue slots from the softmax warps that share its scheduler.
+//   * Warps 0-3 (tile 0) and 4-7 (tile 1) own one TMEM lane (= query row)
 //     each: read the S row, apply the bottom-right mask only on tiles that
 //     reach past the row's last visible key, run the online softmax in base 2
 //     (the running max is only raised, and O rescaled, when it grows by more
 //     than 2^8, which keeps P <= 256 and leaves O/l unchanged), write P as
 //     bf16 into the S columns, and at the end normalise O and store bf16 rows.
-//   * TMEM: 512 columns (S0, S1, O0, O1, 128 each); shared memory: Q0, Q1 and
+//   * TMEM: 512 columns (S0, S1, O0, O1, 128 each); shared memory: Q0, Q1,
 //     two K and two V stages (192 KB).
 #include <algorithm>
 #include <type_traits>
@@ -46,14 +50,17 @@ constexpr int kBN = 128;               // keys per tile
 constexpr int kD = 128;                // head_dim
 constexpr int kSub = 128 * kBM;        // bytes of one 64-dim (128-byte-wide) half of a 128-row tile
 constexpr int kTileBytes = 2 * kSub;   // 32 KB
-constexpr int kStages = 2;             // K/V ring depth
-constexpr int kSmem = 1024 + (2 + 2 * kStages) * kTileBytes;
-constexpr int kThreads = 384;          // 2 x 4 softmax warps, then producer, MMA, 2 idle
+constexpr int kKStages = 2;            // K ring depth
+constexpr int kVStages = 2;            // V ring depth
+constexpr int kSmem = 1024 + (2 + kKStages + kVStages) * kTileBytes;
+static_assert(kSmem <= 227 * 1024, "shared memory over the per-CTA limit");
+static_assert(32 % (kBN / 16) == 0 && 32 % (kBN / 32) == 0, "tiles must not straddle a block-id window");
+constexpr int kThreads = 384;          // 2 x 4 softmax warps, K producer, MMA, V producer, idle
 // Register split (setmaxnreg): launched at 65536/384 -> 168 per thread; the
-// producer/MMA warpgroup drops to 56 so the two softmax warpgroups can hold a
-// whole 128-key score row: 2*128*224 + 128*56 = 384*168.
-constexpr int kSoftmaxRegs = 224;
-constexpr int kControlRegs = 56;
+// producer/MMA warpgroup drops to 72 so the two softmax warpgroups can hold a
+// whole 128-key score row: 2*128*216 + 128*72 = 384*168.
+constexpr int kSoftmaxRegs = 216;
+constexpr int kControlRegs = 72;
 static_assert(2 * 128 * kSoftmaxRegs + 128 * kControlRegs <= kThreads * 168,
               "register split exceeds the launch allocation");
 constexpr uint32_t kTmemCols = 512;
@@ -62,15 +69,15 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units
 // barrier indices
 enum {
   BAR_Q = 0,
-  BAR_KF = 1,   // + stage
-  BAR_KE = 3,   // + stage
-  BAR_VF = 5,   // + stage
-  BAR_VE = 7,   // + stage
-  BAR_S = 9,    // + tile
-  BAR_P = 11,   // + tile
-  BAR_O = 13,   // + tile
-  BAR_DRAIN = 15,
-  NBAR = 16
+  BAR_KF = 1,                  // + stage: K tile landed
+  BAR_KE = BAR_KF + kKStages,  // + stage: K stage free (the S MMAs reading it done)
+  BAR_VF = BAR_KE + kKStages,  // + stage: V tile landed
+  BAR_VE = BAR_VF + kVStages,  // + stage: V stage free (the P.V MMAs reading it done)
+  BAR_S = BAR_VE + kVStages,   // + tile: S_i ready
+  BAR_P = BAR_S + 2,           // + tile: P_i written (4 warps)
+  BAR_O = BAR_P + 2,           // + tile: P_i.V done
+  BAR_DRAIN = BAR_O + 2,
+  NBAR = BAR_DRAIN + 1
 };
 
 // Bounded wait that also gives up when another role of the CTA has aborted.
@@ -152,7 +159,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* const base_ptr = smem_raw + (base - raw);
   auto q_s = [&](int i) { return base + i * kTileBytes; };
   auto k_s = [&](int s) { return base + (2 + s) * kTileBytes; };
-  auto v_s = [&](int s) { return base + (2 + kStages + s) * kTileBytes; };
+  auto v_s = [&](int s) { return base + (2 + kKStages + s) * kTileBytes; };
   const uint32_t bar0 = smem_addr(&bars[0]);
   auto bar = [&](int i) { return bar0 + 8u * i; };
 
@@ -175,10 +182,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp >= 8) {
    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kControlRegs));
-   if (warp == 8) {
-    // ------------------------------------------------------------ producer
-    int k_issued = 0, v_issued = 0;
-    if (lane == 0) {
+   if (warp == 8 || warp == 10) {
+    // ------------------------------------------------------------ producers
+    // warp 8 streams Q and the K tiles, warp 10 the V tiles, each as far
+    // ahead as its own ring allows
+    const bool is_k = warp == 8;
+    const CUtensorMap* map = is_k ? &kmap : &vmap;
+    const int full0 = is_k ? BAR_KF : BAR_VF, empty0 = is_k ? BAR_KE : BAR_VE;
+    const int NS = is_k ? kKStages : kVStages;
+    int issued = 0;
+    if (is_k && lane == 0) {
       mbar_arrive_expect_tx(bar(BAR_Q), (has1 ? 2 : 1) * kTileBytes);
       for (int i = 0; i < (has1 ? 2 : 1); ++i) {
         tma_load_3d(q_s(i), &qmap, bar(BAR_Q), 0, kvh * G, q0 + t00 + i * TPT);
@@ -188,64 +201,56 @@ __global__ void __launch_bounds__(kThreads, 1)
     const long long bt_row = static_cast<long long>(b) * a.max_blocks;
     const int n_keys = min(cached + min(t00 + 2 * TPT, q_len), kv_len);
     const int oob = a.num_blocks * BS;  // first row past the pool: TMA fills zeros
-    for (int n = 0; n < T; ++n) {
-      const int s = n % kStages;
+    // Block ids come 32 at a time (lane l: logical block wb + l, as the pool
+    // row of its first key), the next window's table reads in flight while
+    // the current one is used.
+    auto load_ids = [&](int wb) {
+      const int lb = wb + lane;
       int rc = oob;
-      if (lane < kBlocksPerTile) {
-        const int lb = n * kBlocksPerTile + lane;
-        if (lb * BS < n_keys && lb < a.max_blocks) {
-          const int phys = a.block_tables[bt_row + lb];
-          if (phys >= 0 && phys < a.num_blocks) {
-            rc = phys * BS;
-          } else {
-            report_error(a.err, PA_DEVERR_BLOCK_RANGE);
-          }
+      if (lb * BS < n_keys && lb < a.max_blocks) {
+        const int phys = a.block_tables[bt_row + lb];
+        if (phys >= 0 && phys < a.num_blocks) {
+          rc = phys * BS;
+        } else if (is_k) {
+          report_error(a.err, PA_DEVERR_BLOCK_RANGE);
         }
       }
-      if (n >= kStages &&
-          !warp_wait(bar(BAR_KE + s), ((n - kStages) / kStages) & 1, &abort_flag, a.err))
-        break;
-      if (lane == 0) mbar_arrive_expect_tx(bar(BAR_KF + s), kTileBytes);
+      return rc;
+    };
+    int wbase = 0;
+    int cur_ids = load_ids(0), nxt_ids = load_ids(32);
+    for (int n = 0; n < T; ++n) {
+      const int s = n % NS;
+      if (n * kBlocksPerTile - wbase == 32) {  // tiles never straddle a window
+        wbase += 32;
+        cur_ids = nxt_ids;
+        nxt_ids = load_ids(wbase + 32);
+      }
+      const int id0 = n * kBlocksPerTile - wbase;
+      if (n >= NS && !warp_wait(bar(empty0 + s), ((n - NS) / NS) & 1, &abort_flag, a.err)) break;
+      const uint32_t dst = is_k ? k_s(s) : v_s(s);
+      if (lane == 0) mbar_arrive_expect_tx(bar(full0 + s), kTileBytes);
 #pragma unroll
       for (int i = 0; i < kBlocksPerTile; ++i) {
-        const int c = __shfl_sync(0xffffffffu, rc, i);
+        const int c = __shfl_sync(0xffffffffu, cur_ids, id0 + i);
         if (lane == 0) {
-          tma_load_3d(k_s(s) + i * BS * 128, &kmap, bar(BAR_KF + s), 0, kvh, c);
-          tma_load_3d(k_s(s) + kSub + i * BS * 128, &kmap, bar(BAR_KF + s), 64, kvh, c);
+          tma_load_3d(dst + i * BS * 128, map, bar(full0 + s), 0, kvh, c);
+          tma_load_3d(dst + kSub + i * BS * 128, map, bar(full0 + s), 64, kvh, c);
         }
       }
-      ++k_issued;
-      if (n >= kStages &&
-          !warp_wait(bar(BAR_VE + s), ((n - kStages) / kStages) & 1, &abort_flag, a.err))
-        break;
-      if (lane == 0) mbar_arrive_expect_tx(bar(BAR_VF + s), kTileBytes);
-#pragma unroll
-      for (int i = 0; i < kBlocksPerTile; ++i) {
-        const int c = __shfl_sync(0xffffffffu, rc, i);
-        if (lane == 0) {
-          tma_load_3d(v_s(s) + i * BS * 128, &vmap, bar(BAR_VF + s), 0, kvh, c);
-          tma_load_3d(v_s(s) + kSub + i * BS * 128, &vmap, bar(BAR_VF + s), 64, kvh, c);
-        }
-      }
-      ++v_issued;
+      ++issued;
     }
     if (abort_flag) {
       // let the copies already in flight land before shared memory is released
-      for (int n = max(0, k_issued - kStages); n < k_issued; ++n)
-        (void)mbar_wait(bar(BAR_KF + n % kStages), (n / kStages) & 1);
-      for (int n = max(0, v_issued - kStages); n < v_issued; ++n)
-        (void)mbar_wait(bar(BAR_VF + n % kStages), (n / kStages) & 1);
+      for (int n = max(0, issued - NS); n < issued; ++n)
+        (void)mbar_wait(bar(full0 + n % NS), (n / NS) & 1);
     }
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issue
     constexpr uint32_t kIdescQK = tc::idesc_bf16_f32(kBM, kBN, false, false);
     constexpr uint32_t kIdescPV = tc::idesc_bf16_f32(kBM, kD, false, true);
-    // Order per key tile n: P.V of tile 0, then S of tile 0 for key tile n+1,
-    // then the same for tile 1. Each tile's next S starts as soon as its own
-    // P.V is done, so one tile's softmax runs while the tensor pipe works on
-    // the other tile (S_i and P_i share TMEM columns: S_i(n+1) waits for
-    // P_i V(n) to finish).
-    auto issue_s = [&](int i, int ks) {
+    auto issue_s = [&](int i, int n) {  // S_i = Q_i K(n)^T
+      const int ks = n % kKStages;
       tc::fence_after_sync();
       if (lane == 0) {
 #pragma unroll
@@ -258,7 +263,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
     };
-    auto issue_pv = [&](int i, int vs, int n) {
+    auto issue_pv = [&](int i, int n) {  // O_i += P_i V(n)
+      const int vs = n % kVStages;
       tc::fence_after_sync();
       if (lane == 0) {
 #pragma unroll
@@ -278,10 +284,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
     }
     for (int n = 0; ok && n < T; ++n) {
-      const int s = n % kStages;
-      if (!warp_wait(bar(BAR_VF + s), (n / kStages) & 1, &abort_flag, a.err)) break;
-      // rows of the last, partly filled physical block past kv_len hold
-      // whatever the pool had there: zero them so that P = 0 times V stays 0
+      const int s = n % kVStages;
+      if (!warp_wait(bar(BAR_VF + s), (n / kVStages) & 1, &abort_flag, a.err)) break;
       const int r0 = kv_len - n * kBN;
       if (r0 > 0 && r0 < kBN && (r0 % BS) != 0) {
         const int r1 = min(kBN, (r0 / BS + 1) * BS);
@@ -294,9 +298,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async_smem();
         __syncwarp();
       }
-      const bool more = n + 1 < T;  // tile 1 (the later one) needs key tile n+1
-      const int s1 = (n + 1) % kStages;
-      if (more && !warp_wait(bar(BAR_KF + s1), ((n + 1) / kStages) & 1, &abort_flag, a.err))
+      const bool more = n + 1 < T;
+      const int s1 = (n + 1) % kKStages;
+      if (more && !warp_wait(bar(BAR_KF + s1), ((n + 1) / kKStages) & 1, &abort_flag, a.err))
         break;
       for (int i = 0; i < 2; ++i) {
         if (n >= Tq[i]) continue;
@@ -304,14 +308,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
-        issue_pv(i, s, n);
+        issue_pv(i, n);
         if (n + 1 < Tq[i]) {
-          // S_i / P_i columns are free once this P_i V is done
           if (!warp_wait(bar(BAR_O + i), n & 1, &abort_flag, a.err)) {
             ok = false;
             break;
           }
-          issue_s(i, s1);
+          issue_s(i, n + 1);
         }
       }
       if (!ok) break;

@@ -139,7 +139,7 @@ def _full_size(name):
 
 
 @pytest.mark.parametrize("name", ["llama3_8b_decode_b64", "long_context_decode_b8",
-                                  "llama3_70b_fp8_decode_b256"])
+                                  "llama3_70b_fp8_decode_b256", "llama3_8b_short_decode_b2304"])
 def test_full_size_workload_every_sequence(name):
     # the bench's launch configuration; every output row against the oracle
     got, want = _full_size(name)

@@ -55,6 +55,15 @@ WORKLOADS = {
                                         lens=("lognormal", 1024.0, 1.0, 1, 16384),
                                         pool_factor=1.1, scale=1.0 / math.sqrt(128),
                                         kv_dtype="int8"),
+    # A continuous batch above the persistent decode's limit (2048 sequences):
+    # 2304 mostly short sequences, Llama-3-8B heads, context_len lognormal
+    # (median 96, sigma 1) clipped to [8, 1536]; about 5 % exceed one 512-token
+    # split. Exercises the grid-split decode, its merge and the separate append.
+    "llama3_8b_short_decode_b2304": dict(kind="decode", seed=5, batch=2304, num_heads=32,
+                                         num_kv_heads=8, head_dim=128, block_size=16,
+                                         lens=("lognormal", 96.0, 1.0, 8, 1536),
+                                         pool_factor=1.1, scale=1.0 / math.sqrt(128),
+                                         kv_dtype="bf16"),
     # Varlen prefix-cached prefill: 8 sequences, 32/8 heads, D=128, bs=16,
     # cached_len uniform in [0, 2048], q_len uniform in [128, 1024].
     "varlen_prefill_b8": dict(kind="prefill", seed=4, batch=8, num_heads=32, num_kv_heads=8,
