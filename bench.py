@@ -96,11 +96,19 @@ def prefill_flops(cached, q_lens, num_heads, head_dim) -> int:
     return 4 * head_dim * num_heads * keys
 
 
-def traffic_from_profile(kernel_file: str, workload: str):
+def profile_name(workload: str, window: int = 0) -> str:
+    """The committed ncu summary of a workload's main kernel."""
+    if W.WORKLOADS[workload]["kind"] == "prefill":
+        return f"prefill_kernel_{workload}.md"
+    win = f"window{window}_" if window > 0 else ""
+    return f"decode_persistent_kernel_{win}{workload}.md"
+
+
+def traffic_from_profile(kernel_file: str, workload: str, window: int = 0):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on
     the current kernel source (the summary records the source's sha256)."""
     src = os.path.join(ROOT, "paged_kv_cache_186_gb300", "csrc", kernel_file)
-    prof = os.path.join(ROOT, "profiles", f"decode_persistent_kernel_{workload}.md")
+    prof = os.path.join(ROOT, "profiles", profile_name(workload, window))
     try:
         sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
         text = open(prof).read()
@@ -667,6 +675,8 @@ def other_decode_entry(pa, key, name, dev, args, window, sinks):
                      if fits_l2 else
                      {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                       "frac": achieved / peak, "peak_kind": f"of {peak_kind}",
+                      "traffic": traffic_from_profile("pa_decode.cu", name, window),
+                      "traffic_source": "profiles/" + profile_name(name, window),
                       "kernel": ("decode_persistent_kernel (pa_decode_append: region events / "
                                  "steps)" if b.fused else
                                  "decode_persistent_kernel (pa_decode_window: CUDA events per "
@@ -717,7 +727,7 @@ def run_gpu(args, world, rank, local):
         return
     peak, peak_kind = peaks()
     achieved = step_bytes / (dec_avg_ms / 1e3) / 1e9
-    traffic = traffic_from_profile("pa_decode.cu", name) if args.window <= 0 else None
+    traffic = traffic_from_profile("pa_decode.cu", name, args.window)
     config["parallelism"] = f"replicas x{world} (sequences sharded, no collective)"
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
@@ -734,7 +744,7 @@ def run_gpu(args, world, rank, local):
                      "kernel": ("pa_decode_append (decode_persistent_kernel, the only launch "
                                 "of the timed region: region events / steps)" if fused else
                                 "pa_decode (decode_persistent_kernel, CUDA events per call)"),
-                     "traffic_source": "profiles/decode_persistent_kernel_" + name + ".md",
+                     "traffic_source": "profiles/" + profile_name(name, args.window),
                      "peak_kind": f"of {peak_kind}"},
         "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
@@ -844,6 +854,8 @@ def prefill_entry(pa, name, dev, args):
         "prefill_us": pre_ms * 1e3, "tflops": b.flops / (step_ms / 1e3) / 1e12,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "peak_kind": f"of {kind} (bf16 dense, burst)",
+                     "traffic": traffic_from_profile("pa_prefill.cu", name),
+                     "traffic_source": "profiles/" + profile_name(name),
                      "kernel": "prefill_kernel (CUDA events per call)"},
         "gpu_launches": 2 * steps,
         "config": b.config(),
@@ -887,7 +899,9 @@ def run_prefill(args, world, rank, local):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic", "config": config,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": achieved / peak, "traffic": None,
+                     "frac": achieved / peak,
+                     "traffic": traffic_from_profile("pa_prefill.cu", args.workload),
+                     "traffic_source": "profiles/" + profile_name(args.workload),
                      "kernel": "prefill_kernel (CUDA events per call)",
                      "peak_kind": f"of {kind} (bf16 dense)"},
         "gpu_launches": 2 * args.steps,
