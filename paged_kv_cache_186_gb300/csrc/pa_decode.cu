@@ -589,21 +589,31 @@ __device__ __forceinline__ void write_warp_result(const DecodeArgs& a, int b, in
 
 // Warps that take part: one per kBlocksPerWarp blocks of work (fewer pieces
 // and merges; measured best from batch 4 to 64 at ~2k tokens), but at least
-// one per kMinBlocksPerWarp blocks up to one warp per CTA, so that small
-// problems keep some parallelism, and at most kMaxPartsPerSegment per
-// (sequence, kv head) segment. Segments of more than kGroupedAbove parts
-// merge in two levels, so no warp merges more than max(kGroupedAbove,
-// kMergeGroup + the number of groups) partials. Every active warp owns a
-// non-empty range.
+// one per kMinBlocksPerWarp blocks (one per block for short segments) up to
+// one warp per CTA, so that small problems keep
+// some parallelism, and at most kMaxPartsPerSegment per (sequence, kv head)
+// segment. Segments of more than kGroupedAbove parts merge in two levels, so
+// no warp merges more than max(kGroupedAbove, kMergeGroup + the number of
+// groups) partials. Every active warp owns a non-empty range.
 constexpr int kBlocksPerWarp = 16;
 constexpr int kMinBlocksPerWarp = 4;
 constexpr int kMaxPartsPerSegment = 1024;
 __device__ __forceinline__ long long active_warps(long long N, long long ctas, long long warps,
-                                                  long long segments) {
-  long long w = max(N / kBlocksPerWarp, min(N / kMinBlocksPerWarp, ctas));
+                                                  long long segments, bool one_block_floor) {
+  // (no division by a run-time value: a 64-bit divide here costs registers)
+  long long w = max(N / kBlocksPerWarp, min(one_block_floor ? N : N / kMinBlocksPerWarp, ctas));
   w = min(w, segments * kMaxPartsPerSegment);
   return max(1LL, min(warps, w));
 }
+
+// The floor for a problem whose longest segment has max_blk blocks: when
+// every segment is shorter than 8 blocks, one block per warp (the merge of a
+// few partials costs less than walking several blocks in turn); otherwise
+// kMinBlocksPerWarp. Measured by graph replay on one GB300: the tiny decode
+// (7-block segments) 11.7 -> 6.3 us; one 512-token sequence (32-block
+// segments) 9.45 us at 4 blocks per warp, 13.0 at 1 and 11.1 at 3 (warp
+// ranges then straddle segments unevenly); longer segments unchanged.
+constexpr int kShortSegmentBlocks = 8;
 
 // Pieces of a segment that straddles warps: segment (b, kvh) over global
 // blocks [s0, s1) is split among warps w0 .. w1 (all with non-empty ranges);
@@ -948,7 +958,7 @@ __global__ void __launch_bounds__(NW * 32, 3)
   // ---- this warp's range; from here on warps are independent
   const long long N = static_cast<long long>(prefix[B]) * Hkv;
   const long long W = active_warps(N, gridDim.x, static_cast<long long>(gridDim.x) * NW,
-                                   static_cast<long long>(B) * Hkv);
+                                   static_cast<long long>(B) * Hkv, max_blk < kShortSegmentBlocks);
   const long long gw = static_cast<long long>(blockIdx.x) * NW + warp;
   const long long r0 = gw < W ? gw * N / W : 0, r1 = gw < W ? (gw + 1) * N / W : 0;
   const bool active = r0 < r1;  // warps past W (or with an empty range) only wait
@@ -1426,7 +1436,14 @@ DecodePlan plan_decode(int batch, int num_heads, int num_kv_heads, int head_dim,
   if (batch <= kMaxPersistentBatch) {
     const int per_sm = dispatch(head_dim, block_size, kv,
                                 [&](auto inst) { return decltype(inst)::ctas_per_sm(batch); });
-    p.persistent_ctas = per_sm * num_sms;
+    // No more CTAs than blocks the call can hold (the host-side length
+    // bound): at most one warp per block ever gets work, and a CTA without
+    // any only runs its prologue. Small problems thus launch a small grid.
+    const long long nblk_max = (std::max(len_cap, 0) + block_size - 1) / block_size;
+    const long long blocks_max = static_cast<long long>(batch) * nblk_max * num_kv_heads;
+    const long long ctas_needed = std::max(1LL, blocks_max);
+    p.persistent_ctas = static_cast<int>(std::min<long long>(static_cast<long long>(per_sm) * num_sms,
+                                                             ctas_needed));
     p.blocks_per_split = 0;
     p.num_splits = 0;
     // two partial slots per warp, one row per query head of a group (rounded
