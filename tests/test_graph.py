@@ -159,6 +159,63 @@ def test_captured_decode_replays_grouped_merges():
     _replay_loop(h, inputs, _fused_append, 1, 32)
 
 
+def test_captured_window_and_fp8_decodes_replay_back_to_back():
+    # the sliding-window instantiation and the 8-bit instantiation, each
+    # captured once and replayed with new queries, against the oracle
+    lens = _bench_shaped_lengths(128)
+    for kv, H, Hkv, bs in (("bf16", 32, 8, 16), ("fp8", 64, 8, 32)):
+        h = W.make_decode(64, H, Hkv, 128, bs, lens, seed=129, kv_dtype=kv)
+        g_state = to_device(h)
+        n = pa.decode_workspace_size(g_state.k_cache, 64, H, g_state.block_tables.shape[1],
+                                     k_scale=g_state.k_scale, v_scale=g_state.v_scale)
+        assert n > 0
+        ws = torch.empty(n, dtype=torch.uint8, device="cuda")
+        out = torch.empty((64, H, 128), dtype=torch.bfloat16, device="cuda")
+        q = g_state.q.clone()
+        pa.store_kv(g_state.k_new, g_state.v_new, g_state.slot_mapping, g_state.k_cache,
+                    g_state.v_cache, g_state.k_scale_new, g_state.v_scale_new, g_state.k_scale,
+                    g_state.v_scale)
+        window, sinks = (1024, 4) if kv == "bf16" else (0, 0)
+
+        def run():
+            return pa.decode_window(q, g_state.k_cache, g_state.v_cache, g_state.block_tables,
+                                    g_state.context_lens, g_state.scale, window, sinks, out=out,
+                                    workspace=ws, k_scale=g_state.k_scale, v_scale=g_state.v_scale)
+
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            run()
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            run()
+        # the oracle's cache after the one store
+        if kv == "bf16":
+            kc, vc = W.bf16_bits(h.k_cache).copy(), W.bf16_bits(h.v_cache).copy()
+            oracle.store_kv(W.bf16_bits(h.k_new), W.bf16_bits(h.v_new), h.slot_mapping.numpy(),
+                            kc, vc)
+            ks = vs = None
+        else:
+            kc, vc = W.u8(h.k_cache).copy(), W.u8(h.v_cache).copy()
+            ks, vs = h.k_scale.numpy().copy(), h.v_scale.numpy().copy()
+            oracle.store_kv(W.u8(h.k_new), W.u8(h.v_new), h.slot_mapping.numpy(), kc, vc,
+                            h.k_scale_new.numpy(), h.v_scale_new.numpy(), ks, vs)
+        gen = torch.Generator().manual_seed(130)
+        for r in range(4):
+            qh = torch.randn(q.shape, generator=gen).to(torch.bfloat16)
+            q.copy_(qh)
+            out.fill_(float("nan"))
+            graph.replay()
+            torch.cuda.synchronize()
+            assert pa.get_device_error() == 0
+            want = oracle.decode(W.bf16_bits(qh), kc, vc, h.block_tables.numpy(),
+                                 h.context_lens.numpy(), h.scale, k_scale=ks, v_scale=vs,
+                                 window=window, sinks=sinks)
+            assert_attention_close(out, want, f"{kv} window {window} replay {r}")
+
+
 def test_replays_of_an_unchanged_step_stay_correct():
     # the same inputs every replay: the output must not change between replays
     lens0 = _bench_shaped_lengths(126)
