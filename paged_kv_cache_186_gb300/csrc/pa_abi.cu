@@ -88,26 +88,49 @@ pa_status check_cache(const pa_kv_cache* c) {
 
 int elem_bytes(const pa_kv_cache* c) { return c->dtype == PA_KV_BF16 ? 2 : 1; }
 
-// Tensor map over a cache viewed as 3-D (head_dim, num_kv_heads,
-// num_blocks*block_size), boxes of one 128-byte-wide, block_size-tall tile of
-// one kv head, 128B-swizzled (matching the kernels' shared-memory layout).
-pa_status encode_cache_map(CUtensorMap* map, void* base, const pa_kv_cache* c) {
+// Tensor maps over a cache, 128B-swizzled to match the kernels' shared-memory
+// layouts. A tile is block_size rows of one kv head, stored as 128-byte-wide
+// subtiles one after the other (subtile j holds bytes [128 j, 128 j + 128) of
+// every row).
+//   kind kSubtileMap (prefill): the cache as 3-D (head_dim, num_kv_heads,
+//     num_blocks*block_size); one box is one subtile.
+//   kind kRowMap (decode): the cache as 4-D (128 bytes of a row, row,
+//     subtile, kv head), box (128 bytes, block_size, all subtiles, 1): one box
+//     is a whole tile, one copy instead of one per subtile.
+constexpr int kSubtileMap = 0, kRowMap = 1;
+pa_status encode_cache_map(CUtensorMap* map, void* base, const pa_kv_cache* c, int kind) {
   const int eb = elem_bytes(c);
-  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(c->head_dim),
-                              static_cast<cuuint64_t>(c->num_kv_heads),
-                              static_cast<cuuint64_t>(c->num_blocks) * c->block_size};
-  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(c->head_dim) * eb,
-                                 static_cast<cuuint64_t>(c->head_dim) * eb * c->num_kv_heads};
-  const cuuint32_t box[3] = {static_cast<cuuint32_t>(pa::kSwizzleBytes / eb), 1u,
-                             static_cast<cuuint32_t>(c->block_size)};
-  const cuuint32_t estr[3] = {1u, 1u, 1u};
-  const CUresult r = g_encode(
-      map, eb == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base,
-      dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-      // rows are head_dim*elem bytes apart from the next head's: promote L2
-      // fills no wider than one row so no neighbouring head is fetched
-      eb == 1 ? CU_TENSOR_MAP_L2_PROMOTION_L2_128B : CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  const cuuint64_t row_bytes = static_cast<cuuint64_t>(c->head_dim) * eb;
+  const cuuint64_t rows = static_cast<cuuint64_t>(c->num_blocks) * c->block_size;
+  const CUtensorMapDataType dt =
+      eb == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  // rows are head_dim*elem bytes apart from the next head's: promote L2
+  // fills no wider than one row so no neighbouring head is fetched
+  const CUtensorMapL2promotion promo =
+      eb == 1 ? CU_TENSOR_MAP_L2_PROMOTION_L2_128B : CU_TENSOR_MAP_L2_PROMOTION_L2_256B;
+  CUresult r;
+  if (kind == kSubtileMap) {
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(c->head_dim),
+                                static_cast<cuuint64_t>(c->num_kv_heads), rows};
+    const cuuint64_t strides[2] = {row_bytes, row_bytes * c->num_kv_heads};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(pa::kSwizzleBytes / eb), 1u,
+                               static_cast<cuuint32_t>(c->block_size)};
+    const cuuint32_t estr[3] = {1u, 1u, 1u};
+    r = g_encode(map, dt, 3, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                 CU_TENSOR_MAP_SWIZZLE_128B, promo, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  } else {
+    const cuuint64_t nsub = row_bytes / pa::kSwizzleBytes;
+    const cuuint64_t dims[4] = {static_cast<cuuint64_t>(pa::kSwizzleBytes / eb), rows, nsub,
+                                static_cast<cuuint64_t>(c->num_kv_heads)};
+    const cuuint64_t strides[3] = {row_bytes * c->num_kv_heads,
+                                   static_cast<cuuint64_t>(pa::kSwizzleBytes), row_bytes};
+    const cuuint32_t box[4] = {static_cast<cuuint32_t>(pa::kSwizzleBytes / eb),
+                               static_cast<cuuint32_t>(c->block_size),
+                               static_cast<cuuint32_t>(nsub), 1u};
+    const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+    r = g_encode(map, dt, 4, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                 CU_TENSOR_MAP_SWIZZLE_128B, promo, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  }
   return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
 }
 
@@ -115,7 +138,7 @@ pa_status encode_cache_map(CUtensorMap* map, void* base, const pa_kv_cache* c) {
 // few microseconds, and a decode loop passes the same cache every step.
 struct MapEntry {
   void* base;
-  int num_blocks, block_size, num_kv_heads, head_dim, dtype, device;
+  int num_blocks, block_size, num_kv_heads, head_dim, dtype, device, kind;
   CUtensorMap map;
 };
 constexpr int kMapCache = 16;
@@ -123,7 +146,7 @@ MapEntry g_maps[kMapCache];
 int g_map_count = 0, g_map_next = 0;
 std::mutex g_map_mu;
 
-pa_status cached_cache_map(CUtensorMap* out, void* base, const pa_kv_cache* c) {
+pa_status cached_cache_map(CUtensorMap* out, void* base, const pa_kv_cache* c, int kind) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return PA_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_map_mu);
@@ -131,13 +154,14 @@ pa_status cached_cache_map(CUtensorMap* out, void* base, const pa_kv_cache* c) {
     const MapEntry& e = g_maps[i];
     if (e.base == base && e.num_blocks == c->num_blocks && e.block_size == c->block_size &&
         e.num_kv_heads == c->num_kv_heads && e.head_dim == c->head_dim && e.dtype == c->dtype &&
-        e.device == dev) {
+        e.device == dev && e.kind == kind) {
       *out = e.map;
       return PA_OK;
     }
   }
-  MapEntry e{base, c->num_blocks, c->block_size, c->num_kv_heads, c->head_dim, c->dtype, dev, {}};
-  const pa_status st = encode_cache_map(&e.map, base, c);
+  MapEntry e{base, c->num_blocks, c->block_size, c->num_kv_heads, c->head_dim, c->dtype, dev,
+             kind, {}};
+  const pa_status st = encode_cache_map(&e.map, base, c, kind);
   if (st != PA_OK) return st;
   g_maps[g_map_next] = e;
   g_map_next = (g_map_next + 1) % kMapCache;
@@ -270,8 +294,8 @@ pa_status decode_common(const void* q, const pa_kv_cache* cache, const int32_t* 
     return PA_ERR_WORKSPACE;
   if (window > 0 && plan.persistent_ctas == 0) return PA_ERR_UNSUPPORTED;
   CUtensorMap kmap, vmap;
-  if ((st = cached_cache_map(&kmap, cache->k_cache, cache)) != PA_OK) return st;
-  if ((st = cached_cache_map(&vmap, cache->v_cache, cache)) != PA_OK) return st;
+  if ((st = cached_cache_map(&kmap, cache->k_cache, cache, kRowMap)) != PA_OK) return st;
+  if ((st = cached_cache_map(&vmap, cache->v_cache, cache, kRowMap)) != PA_OK) return st;
   const cudaStream_t strm = static_cast<cudaStream_t>(stream);
   const bool fused_append = k_new != nullptr && plan.persistent_ctas > 0;
   if (k_new != nullptr && !fused_append) {
@@ -428,8 +452,8 @@ pa_status pa_prefill_varlen(const void* q, const pa_kv_cache* cache, const int32
                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return PA_ERR_CUDA;
   }
-  if ((st = cached_cache_map(&kmap, cache->k_cache, cache)) != PA_OK) return st;
-  if ((st = cached_cache_map(&vmap, cache->v_cache, cache)) != PA_OK) return st;
+  if ((st = cached_cache_map(&kmap, cache->k_cache, cache, kSubtileMap)) != PA_OK) return st;
+  if ((st = cached_cache_map(&vmap, cache->v_cache, cache, kSubtileMap)) != PA_OK) return st;
   pa::PrefillArgs a{};
   a.block_tables = block_tables;
   a.cu_q = cu_seqlens_q;

@@ -59,7 +59,10 @@ struct Cfg {
   static constexpr int kScaleBytes = Q8 ? NW * ST * 2 * BS * 4 : 0;
   static constexpr int kMoStride = D + 4;                      // padded row of the merge buffer
   static constexpr int kMerge = NW * 8 * kMoStride * 4 + NW * 8 * 2 * 4;
-  static constexpr uint32_t kTx = kStage + (Q8 ? 2 * BS * 4 : 0);
+  static constexpr uint32_t kTx = kStage;  // bytes the two tensor copies of a stage bring
+  // arrivals per stage phase: the copy issuer's, plus (8-bit) one per lane for
+  // its asynchronous copies of the block's scales
+  static constexpr uint32_t kArrivals = Q8 ? 33 : 1;
   static_assert(kRowBytes % kSwizzleBytes == 0, "row must be a multiple of 128 bytes");
   static_assert(BS % 16 == 0, "block size must be a multiple of 16");
   static_assert(!Q8 || D == 128, "the 8-bit path is written for head_dim 128");
@@ -72,6 +75,23 @@ template <int BS>
 __device__ __forceinline__ uint32_t swz(uint32_t tile, int row, int chunk) {
   const int sub = chunk >> 3, c = chunk & 7;
   return tile + sub * (BS * kSwizzleBytes) + row * kSwizzleBytes + ((c ^ (row & 7)) << 4);
+}
+
+// The 8-bit scales of one block (BS K scales, then BS V scales, from element
+// `off` of k_scale / v_scale) into shared memory at `dst`: one 4-byte
+// asynchronous copy per lane and scale (no TMA: a 128-byte bulk copy costs the
+// tensor-copy unit as much as a whole tile), then every lane's one arrival on
+// the stage barrier for its copies (the barrier counts 32 of them).
+template <int BS>
+__device__ __forceinline__ void copy_scales(const DecodeArgs& a, uint32_t dst, long long off,
+                                            uint32_t bar, int lane) {
+#pragma unroll
+  for (int i = lane; i < 2 * BS; i += 32) {
+    const bool isv = i >= BS;
+    const int t = isv ? i - BS : i;
+    cp_async_4(dst + 4 * i, (isv ? a.v_scale : a.k_scale) + off + t);
+  }
+  cp_async_arrive_noinc(bar);
 }
 
 // floor(log2 |x|) of a normal float, and 2^k for k in [-126, 127], exactly.
@@ -973,7 +993,7 @@ __global__ void __launch_bounds__(NW * 32, 3)
   // lengths, q and split partials that later reads want from L2
   const uint64_t l2_policy = l2_evict_first_policy();
   if (active && lane == 0) {
-    for (int s = 0; s < ST; ++s) mbar_init(bar0 + 8 * s, 1);
+    for (int s = 0; s < ST; ++s) mbar_init(bar0 + 8 * s, C::kArrivals);
     fence_barrier_init();
     fence_proxy_async_smem();
   }
@@ -1042,23 +1062,18 @@ __global__ void __launch_bounds__(NW * 32, 3)
       if (lane == 0) report_error(a.err, PA_DEVERR_BLOCK_RANGE);
       phys = 0;  // stay inside the pool; the result is flagged as invalid
     }
-    if (lane == 0 && issued != skip_copy) {
+    if (issued != skip_copy) {
       const int s = issued % ST;
       const uint32_t bar = bar0 + 8 * s;
-      const uint32_t kt = stage0 + s * C::kStage;
-      mbar_arrive_expect_tx(bar, C::kTx);
-#pragma unroll
-      for (int j = 0; j < C::kNSub; ++j) {
-        tma_load_3d(kt + j * C::kSubBytes, &kmap, bar, j * (kSwizzleBytes / C::kElem), kvh,
-                    phys * BS, l2_policy);
-        tma_load_3d(kt + C::kTile + j * C::kSubBytes, &vmap, bar,
-                    j * (kSwizzleBytes / C::kElem), kvh, phys * BS, l2_policy);
-      }
-      if constexpr (Q8) {
-        const long long off = (static_cast<long long>(phys) * Hkv + kvh) * BS;
-        const uint32_t sc = scale_base + ((warp * ST + s) * 2) * BS * 4;
-        bulk_load(sc, a.k_scale + off, BS * 4, bar, l2_policy);
-        bulk_load(sc + BS * 4, a.v_scale + off, BS * 4, bar, l2_policy);
+      if constexpr (Q8)
+        copy_scales<BS>(a, scale_base + ((warp * ST + s) * 2) * BS * 4,
+                        (static_cast<long long>(phys) * Hkv + kvh) * BS, bar, lane);
+      if (lane == 0) {
+        // the K and V tiles, one tensor copy each (all 128-byte subtiles)
+        const uint32_t kt = stage0 + s * C::kStage;
+        mbar_arrive_expect_tx(bar, C::kTx);
+        tma_load_4d(kt, &kmap, bar, 0, phys * BS, 0, kvh, l2_policy);
+        tma_load_4d(kt + C::kTile, &vmap, bar, 0, phys * BS, 0, kvh, l2_policy);
       }
     }
     ++issued;
@@ -1197,7 +1212,7 @@ __global__ void __launch_bounds__(NW * 32)
   const uint32_t bar0 = smem_addr(&bars[warp * ST]);
   const uint32_t stage0 = base + warp * ST * C::kStage;
   if (lane == 0) {
-    for (int s = 0; s < ST; ++s) mbar_init(bar0 + 8 * s, 1);
+    for (int s = 0; s < ST; ++s) mbar_init(bar0 + 8 * s, C::kArrivals);
     fence_barrier_init();
     fence_proxy_async_smem();
   }
@@ -1205,24 +1220,16 @@ __global__ void __launch_bounds__(NW * 32)
 
   auto issue = [&](int i) {
     const int phys = __shfl_sync(kFull, my_phys, i);
+    const int s = i % ST;
+    const uint32_t bar = bar0 + 8 * s;
+    if constexpr (Q8)
+      copy_scales<BS>(a, scale_base + ((warp * ST + s) * 2) * BS * 4,
+                      (static_cast<long long>(phys) * a.num_kv_heads + kvh) * BS, bar, lane);
     if (lane == 0) {
-      const int s = i % ST;
-      const uint32_t bar = bar0 + 8 * s;
       const uint32_t kt = stage0 + s * C::kStage;
       mbar_arrive_expect_tx(bar, C::kTx);
-#pragma unroll
-      for (int j = 0; j < C::kNSub; ++j) {
-        tma_load_3d(kt + j * C::kSubBytes, &kmap, bar, j * (kSwizzleBytes / C::kElem), kvh,
-                    phys * BS);
-        tma_load_3d(kt + C::kTile + j * C::kSubBytes, &vmap, bar,
-                    j * (kSwizzleBytes / C::kElem), kvh, phys * BS);
-      }
-      if constexpr (Q8) {
-        const long long off = (static_cast<long long>(phys) * a.num_kv_heads + kvh) * BS;
-        const uint32_t sc = scale_base + ((warp * ST + s) * 2) * BS * 4;
-        bulk_load(sc, a.k_scale + off, BS * 4, bar);
-        bulk_load(sc + BS * 4, a.v_scale + off, BS * 4, bar);
-      }
+      tma_load_4d(kt, &kmap, bar, 0, phys * BS, 0, kvh);
+      tma_load_4d(kt + C::kTile, &vmap, bar, 0, phys * BS, 0, kvh);
     }
   };
 
