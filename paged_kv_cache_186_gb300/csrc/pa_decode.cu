@@ -1110,6 +1110,8 @@ __global__ void __launch_bounds__(NW * 32, 3)
 #pragma unroll
     for (int mt = 0; mt < D / 16; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
     float m_run = -INFINITY, l_run = 0.f, vfac = 1.f;
+    const bool whole = cp.lo == 0 && cp.hi == cp.nblk;
+    unsigned long long seen = 0ull;  // the segment's arrival counter near the piece's end
     for (int vb = cp.lo; vb < cp.hi; ++vb) {
       const int blk = sw.logical(vb);  // visible block -> logical block
       const int s = consumed % ST;
@@ -1129,6 +1131,8 @@ __global__ void __launch_bounds__(NW * 32, 3)
       attend_block<D, BS, KV, WIN>(kt, kt + C::kTile, base_ptr, base, ksc, ksc + BS, blk * BS, L,
                                     sw.hole_lo, sw.hole_hi, qa, acc, m_run, l_run, vfac, sl2p,
                                     lane);
+      if (!whole && vb == cp.hi - 1 && lane == 0)
+        seen = ld_relaxed_gpu(a.seg_counters + static_cast<long long>(cp.b) * Hkv + cp.kvh);
       ++consumed;
       __syncwarp();
       issue_pending();
@@ -1138,14 +1142,30 @@ __global__ void __launch_bounds__(NW * 32, 3)
     Piece nx = cp;
     piece_next(nx, prefix, B, Hkv, r1);
     if (nx.valid) fetch_q<D, Q8>(a, nx.b, nx.kvh, lane, qraw);
-    const bool whole = cp.lo == 0 && cp.hi == cp.nblk;
     write_warp_result<D, Q8>(a, cp.b, cp.kvh, whole, 2 * gw + (cp.lo == 0 ? 1 : 0), lane, m_run,
                               l_run, 1.f / vfac, acc);
     if (!whole) {
+      const SegParts sp = seg_parts(prefix, B, Hkv, cp.b, cp.kvh, W);
+      // Every other part already arrived (counted after publishing its
+      // partial): this warp is the segment's last. Its own partial is read
+      // only by its own lanes, so it needs neither a fence nor an arrival:
+      // the counter is cleared for the next call, a fence orders the other
+      // parts' partials before the merge reads them.
+      const bool all_others = sp.n <= kGroupedAbove &&
+                              __shfl_sync(kFull, static_cast<uint32_t>(seen >> 32) == a.epoch &&
+                                                     static_cast<uint32_t>(seen) + 1u ==
+                                                         static_cast<uint32_t>(sp.n), 0);
+      if (all_others) {
+        if (lane == 0) atomicExch(a.seg_counters + static_cast<long long>(cp.b) * Hkv + cp.kvh, 0ull);
+        __threadfence();
+        __syncwarp();
+        merge_segment<D>(a, PartList{sp, 0, 1, sp.n}, cp.b, cp.kvh, true, lane);
+        cp = nx;
+        continue;
+      }
       // publish the partial, count the arrival; the last warp merges the segment
       __threadfence();
       __syncwarp();
-      const SegParts sp = seg_parts(prefix, B, Hkv, cp.b, cp.kvh, W);
       if (sp.n > kGroupedAbove) {
         finish_grouped<D>(a, sp, cp.b, cp.kvh, gw, lane);
       } else {

@@ -285,6 +285,14 @@ __device__ __forceinline__ void grid_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// Relaxed atomic 64-bit load at GPU scope (no ordering by itself; a fence
+// after it makes it an acquire).
+__device__ __forceinline__ unsigned long long ld_relaxed_gpu(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
 __device__ __forceinline__ void report_error(uint32_t* err, uint32_t bit) {
   if (err) atomicOr(err, bit);
 }
