@@ -498,9 +498,11 @@ __device__ __forceinline__ SeqWindow seq_window(int L, int window, int sinks) {
 
 // ============================================================ persistent path
 // Flattened work: segment (b, kvh) in b-major order holds nblk(b) blocks; the
-// global index of its first block is prefix[b] * Hkv + kvh * nblk(b). Warp w
-// of all W = gridDim.x * NW warps owns blocks [w*N/W, (w+1)*N/W) with
-// N = prefix[B] * Hkv: equal work per warp whatever the length mix.
+// global index of its first block is prefix[b] * Hkv + kvh * nblk(b). Each of
+// the W active warps owns a contiguous range of these N = prefix[B] * Hkv
+// blocks, cut so that every warp gets the same work counted in blocks plus a
+// fixed cost per segment end (block_at_unit below): equal work per warp
+// whatever the length mix.
 struct Piece {
   int b, kvh, lo, hi;  // segment and its block range owned by this warp
   int nblk;            // blocks of the segment
@@ -614,7 +616,8 @@ __device__ __forceinline__ void write_warp_result(const DecodeArgs& a, int b, in
 // some parallelism, and at most kMaxPartsPerSegment per (sequence, kv head)
 // segment. Segments of more than kGroupedAbove parts merge in two levels, so
 // no warp merges more than max(kGroupedAbove, kMergeGroup + the number of
-// groups) partials. Every active warp owns a non-empty range.
+// groups) partials. (A warp whose share of the work units holds no block
+// has nothing to do.)
 constexpr int kBlocksPerWarp = 16;
 constexpr int kMinBlocksPerWarp = 4;
 constexpr int kMaxPartsPerSegment = 1024;
@@ -663,15 +666,50 @@ struct PartList {
 };
 
 __device__ __forceinline__ SegParts seg_parts(const int* prefix, int B, int Hkv, int b, int kvh,
-                                              long long W) {
-  const long long N = static_cast<long long>(prefix[B]) * Hkv;
+                                              long long W, int cost) {
+  const long long NU = (static_cast<long long>(prefix[B]) + static_cast<long long>(cost) * B) * Hkv;
   const int nblk = prefix[b + 1] - prefix[b];
-  const long long s0 = static_cast<long long>(prefix[b]) * Hkv + static_cast<long long>(kvh) * nblk;
-  auto owner = [&](long long x) { return ((x + 1) * W - 1) / N; };
+  // unit of the segment's first block
+  const long long u0 = (static_cast<long long>(prefix[b]) + static_cast<long long>(cost) * b) * Hkv +
+                       static_cast<long long>(kvh) * (nblk + cost);
+  auto owner = [&](long long x) { return ((x + 1) * W - 1) / NU; };
   SegParts sp;
-  sp.w0 = owner(s0);
-  sp.n = static_cast<int>(owner(s0 + nblk - 1) - sp.w0 + 1);
+  sp.w0 = owner(u0);
+  sp.n = static_cast<int>(owner(u0 + nblk - 1) - sp.w0 + 1);
   return sp;
+}
+
+// Fixed work at a segment's end (the new token's append, the piece's result
+// or partial, a merge), in blocks of the instantiation's layout. Measured on
+// one GB300 by sweeping the value: Llama-3-8B-shaped batch 64 (bf16, 16-token
+// blocks) 92.9 us at 2, 90.4 at 6, 91.2 at 12; 70B-shaped batch 256 (32-token
+// blocks) best at 4 for E4M3 codes and 3 for INT8 (the widening costs more
+// per block, so the fixed work weighs less); 0 would be the equal-block split.
+__host__ __device__ constexpr int segment_cost(int kv) {
+  return kv == kKvBf16 ? 6 : kv == kKvE4m3 ? 4 : 3;
+}
+
+// The split in work units: segment (b, kvh) is its nblk blocks followed by
+// `cost` units that stand for the fixed work of a segment's end (the new
+// token's append, the piece's result, a merge), so that warps which end many
+// segments get fewer blocks. Warp w owns units [w NU / W, (w+1) NU / W), i.e.
+// the blocks whose units fall there: a contiguous range of the flattened
+// block list. This maps a unit to the index of the first block at or after it.
+__device__ __forceinline__ long long block_at_unit(const int* prefix, int B, int Hkv, int cost,
+                                                   long long u) {
+  const long long NU = (static_cast<long long>(prefix[B]) + static_cast<long long>(cost) * B) * Hkv;
+  if (u >= NU) return static_cast<long long>(prefix[B]) * Hkv;
+  int lo = 0, hi = B - 1;  // last b whose units start at or before u
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if ((static_cast<long long>(prefix[mid]) + static_cast<long long>(cost) * mid) * Hkv <= u) lo = mid;
+    else hi = mid - 1;
+  }
+  const int nb = prefix[lo + 1] - prefix[lo];
+  const long long off = u - (static_cast<long long>(prefix[lo]) + static_cast<long long>(cost) * lo) * Hkv;
+  const int per = nb + cost;
+  const int kvh = static_cast<int>(off / per), pos = static_cast<int>(off % per);
+  return static_cast<long long>(prefix[lo]) * Hkv + static_cast<long long>(kvh) * nb + min(pos, nb);
 }
 
 // Epoch-tagged counters in the caller's workspace (contents on entry are
@@ -980,8 +1018,13 @@ __global__ void __launch_bounds__(NW * 32, 3)
   const long long W = active_warps(N, gridDim.x, static_cast<long long>(gridDim.x) * NW,
                                    static_cast<long long>(B) * Hkv, max_blk < kShortSegmentBlocks);
   const long long gw = static_cast<long long>(blockIdx.x) * NW + warp;
-  const long long r0 = gw < W ? gw * N / W : 0, r1 = gw < W ? (gw + 1) * N / W : 0;
-  const bool active = r0 < r1;  // warps past W (or with an empty range) only wait
+  // segment-end cost of the split, in blocks; none when every segment is
+  // short (one block per warp there)
+  const int cost = max_blk < kShortSegmentBlocks ? 0 : segment_cost(KV);
+  const long long NU = (static_cast<long long>(prefix[B]) + static_cast<long long>(cost) * B) * Hkv;
+  const long long r0 = gw < W ? block_at_unit(prefix, B, Hkv, cost, gw * NU / W) : 0;
+  const long long r1 = gw < W ? block_at_unit(prefix, B, Hkv, cost, (gw + 1) * NU / W) : 0;
+  const bool active = r0 < r1;  // warps past W, or whose units hold no block, have nothing to do
   // a segment of nblk blocks has at most (nblk - 1) W / N + 2 parts: only
   // with a segment of more than kGroupedAbove parts are the group counters used
   const bool may_group =
@@ -1145,7 +1188,7 @@ __global__ void __launch_bounds__(NW * 32, 3)
     write_warp_result<D, Q8>(a, cp.b, cp.kvh, whole, 2 * gw + (cp.lo == 0 ? 1 : 0), lane, m_run,
                               l_run, 1.f / vfac, acc);
     if (!whole) {
-      const SegParts sp = seg_parts(prefix, B, Hkv, cp.b, cp.kvh, W);
+      const SegParts sp = seg_parts(prefix, B, Hkv, cp.b, cp.kvh, W, cost);
       // Every other part already arrived (counted after publishing its
       // partial): this warp is the segment's last. Its own partial is read
       // only by its own lanes, so it needs neither a fence nor an arrival:

@@ -158,6 +158,17 @@ def test_many_short_and_empty_sequences():
     assert_attention_close(got, want, "short/empty")
 
 
+@pytest.mark.parametrize("kv,H,bs", [("bf16", 32, 16), ("fp8", 64, 32), ("int8", 64, 32)])
+def test_empty_sequences_between_long_ones(kv, H, bs):
+    # segments long enough for the split to count a cost per segment end,
+    # with empty sequences (work units but no blocks) between them, in runs
+    lens = [0, 0, 0, 700, 0, 4100, 0, 0, 0, 0, 33, 2500, 0, 1, 0, 0, 9000, 0]
+    h = W.make_decode(len(lens), H, 8, 128, bs, lens, seed=88, kv_dtype=kv)
+    got, want = run_case(h)
+    assert torch.all(got[torch.tensor(lens) == 0].float() == 0)
+    assert_attention_close(got, want, f"empty between long ({kv})")
+
+
 def test_one_long_sequence_spread_over_all_ctas():
     h = W.make_decode(1, 32, 8, 128, 16, [70001], seed=92)
     got, want = run_case(h, max_context_len=70001)
