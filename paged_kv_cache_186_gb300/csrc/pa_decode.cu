@@ -336,8 +336,17 @@ __device__ __forceinline__ void attend_block(uint32_t kt, uint32_t vt, const uin
     }
     const float p0 = pr[4 * hg], p1 = pr[4 * hg + 1], p8 = pr[4 * hg + 2], p9 = pr[4 * hg + 3];
     if constexpr (!Q8) {
+      // P as two bf16 terms, p = hi + lo (hi = bf16(p), lo = bf16(p - hi)):
+      // one bf16 rounding of P alone (2^-9 relative per weight) can move an
+      // output over few keys by more than the tolerance; the sum of two
+      // terms carries ~16 significant bits. The second MMA reuses the V
+      // fragments; this kernel is HBM-bound, the tensor pipe mostly idle.
       const uint32_t pb0 = pack_bf16x2(p0, p1);
       const uint32_t pb1 = pack_bf16x2(p8, p9);
+      const uint32_t pl0 = pack_bf16x2(p0 - __uint_as_float(pb0 << 16),
+                                       p1 - __uint_as_float(pb0 & 0xffff0000u));
+      const uint32_t pl1 = pack_bf16x2(p8 - __uint_as_float(pb1 << 16),
+                                       p9 - __uint_as_float(pb1 & 0xffff0000u));
       const int mi = lane >> 3;
       const int row = hg * 16 + (mi >> 1) * 8 + (lane & 7);
       if (partial) {
@@ -345,7 +354,12 @@ __device__ __forceinline__ void attend_block(uint32_t kt, uint32_t vt, const uin
         for (int mt = 0; mt < D / 16; ++mt) {
           uint32_t a0, a1, a2, a3;
           ldmatrix_x4_trans(swz<BS>(vt, row, 2 * mt + (mi & 1)), a0, a1, a2, a3);
-          mma_bf16(acc[mt], a0 & mlo, a1 & mlo, a2 & mhi, a3 & mhi, pb0, pb1);
+          a0 &= mlo;
+          a1 &= mlo;
+          a2 &= mhi;
+          a3 &= mhi;
+          mma_bf16(acc[mt], a0, a1, a2, a3, pb0, pb1);
+          mma_bf16(acc[mt], a0, a1, a2, a3, pl0, pl1);
         }
       } else {
 #pragma unroll
@@ -353,6 +367,7 @@ __device__ __forceinline__ void attend_block(uint32_t kt, uint32_t vt, const uin
           uint32_t a0, a1, a2, a3;
           ldmatrix_x4_trans(swz<BS>(vt, row, 2 * mt + (mi & 1)), a0, a1, a2, a3);
           mma_bf16(acc[mt], a0, a1, a2, a3, pb0, pb1);
+          mma_bf16(acc[mt], a0, a1, a2, a3, pl0, pl1);
         }
       }
     } else {

@@ -55,13 +55,21 @@ WORKLOADS = {
                                         lens=("lognormal", 1024.0, 1.0, 1, 16384),
                                         pool_factor=1.1, scale=1.0 / math.sqrt(128),
                                         kv_dtype="int8"),
-    # A continuous batch above the persistent decode's limit (2048 sequences):
-    # 2304 mostly short sequences, Llama-3-8B heads, context_len lognormal
-    # (median 96, sigma 1) clipped to [8, 1536]; about 5 % exceed one 512-token
-    # split. Exercises the grid-split decode, its merge and the separate append.
+    # A large continuous batch: 2304 mostly short sequences, Llama-3-8B heads,
+    # context_len lognormal (median 96, sigma 1) clipped to [8, 1536]. The
+    # persistent decode at 2 CTAs per SM (its per-sequence prefix sums take
+    # 9 KB of shared memory per CTA).
     "llama3_8b_short_decode_b2304": dict(kind="decode", seed=5, batch=2304, num_heads=32,
                                          num_kv_heads=8, head_dim=128, block_size=16,
                                          lens=("lognormal", 96.0, 1.0, 8, 1536),
+                                         pool_factor=1.1, scale=1.0 / math.sqrt(128),
+                                         kv_dtype="bf16"),
+    # More sequences than the persistent decode's per-sequence prefix sums
+    # hold (8192): the grid-split decode. Llama-3-8B heads, short contexts
+    # (lognormal, median 64, sigma 0.5, clipped to [8, 512]).
+    "llama3_8b_short_decode_b9216": dict(kind="decode", seed=6, batch=9216, num_heads=32,
+                                         num_kv_heads=8, head_dim=128, block_size=16,
+                                         lens=("lognormal", 64.0, 0.5, 8, 512),
                                          pool_factor=1.1, scale=1.0 / math.sqrt(128),
                                          kv_dtype="bf16"),
     # Varlen prefix-cached prefill: 8 sequences, 32/8 heads, D=128, bs=16,
