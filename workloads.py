@@ -57,8 +57,8 @@ WORKLOADS = {
                                         kv_dtype="int8"),
     # A large continuous batch: 2304 mostly short sequences, Llama-3-8B heads,
     # context_len lognormal (median 96, sigma 1) clipped to [8, 1536]. The
-    # persistent decode at 2 CTAs per SM (its per-sequence prefix sums take
-    # 9 KB of shared memory per CTA).
+    # persistent decode with 9 KB of per-sequence prefix sums in each CTA's
+    # shared memory.
     "llama3_8b_short_decode_b2304": dict(kind="decode", seed=5, batch=2304, num_heads=32,
                                          num_kv_heads=8, head_dim=128, block_size=16,
                                          lens=("lognormal", 96.0, 1.0, 8, 1536),
