@@ -11,16 +11,17 @@
 // How (GB300 design):
 //   * Work is the list of (sequence, kv head) "segments", each a run of
 //     ceil(context_len / bs) physical blocks. The persistent kernel gives every
-//     warp an equal contiguous share of all blocks of all segments (a balanced
-//     split: long and short sequences cost the same per block, and no CTA is
-//     launched without work). A warp writes the bf16 rows of a segment it holds
-//     whole; for a segment that straddles warps each writes an fp32 partial
-//     and the last to arrive (per-segment counter) merges them.
+//     warp a contiguous share of all blocks of all segments, equal in work
+//     units (each block one unit, each segment end a fixed number more): long
+//     and short sequences cost the same per block, and no CTA is launched
+//     without work. A warp writes the bf16 rows of a segment it holds whole;
+//     for a segment that straddles warps each writes an fp32 partial and the
+//     last to arrive (per-segment counter) merges them.
 //   * All G = H/Hkv query heads of a kv head share every K/V tile (GQA).
 //   * Each warp streams its blocks through a private ring of shared-memory
-//     stages filled by TMA (3-D tiled loads of one block of one kv head,
-//     128B-swizzled; 8-bit-code scales by 1-D bulk copies), tracked by
-//     mbarriers with bounded waits. Loads run ahead across segment boundaries;
+//     stages filled by TMA (one tensor copy per K or V tile of one block and
+//     kv head, 128B-swizzled; 8-bit-code scales by per-lane 4-byte async
+//     copies), tracked by mbarriers with bounded waits. Loads run ahead across segment boundaries;
 //     block ids are read 32 at a time, a window ahead of the loads.
 //   * The two contractions per block, S = Q K^T (heads x tokens over head_dim)
 //     and O^T += V^T P^T (head_dim x heads over tokens), run on the warp-level

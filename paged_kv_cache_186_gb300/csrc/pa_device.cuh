@@ -93,16 +93,6 @@ __device__ __forceinline__ uint64_t l2_evict_first_policy() {
   return p;
 }
 
-// tma_load_3d with an L2 cache policy (from createpolicy).
-__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
-                                            int c0, int c1, int c2, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      ".L2::cache_hint [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "l"(policy)
-      : "memory");
-}
-
 // 4-D tiled tensor load with an L2 cache policy, completing on `bar`.
 __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
                                             int c0, int c1, int c2, int c3, uint64_t policy) {
@@ -134,44 +124,6 @@ __device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src) {
 // must include one per thread that makes this call in a phase.
 __device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
-}
-
-// Plain bulk copy global -> shared (both 16-byte aligned, bytes % 16 == 0).
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
-                                          uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
-          "r"(dst),
-      "l"(src), "r"(bytes), "r"(bar)
-      : "memory");
-}
-
-// bulk_load with an L2 cache policy.
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
-                                          uint32_t bar, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
-      " [%0], [%1], %2, [%3], %4;" ::"r"(dst),
-      "l"(src), "r"(bytes), "r"(bar), "l"(policy)
-      : "memory");
-}
-
-// Bring one 3-D tile into L2 only (no shared memory, no completion).
-__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* map, int c0, int c1, int c2) {
-  asm volatile(
-      "cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
-          reinterpret_cast<uint64_t>(map)),
-      "r"(c0), "r"(c1), "r"(c2)
-      : "memory");
-}
-
-// Bring `bytes` (multiple of 16, 16-byte aligned) into L2 only.
-__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
-}
-
-__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
-  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
 // ---------------------------------------------------------------- warp MMA
@@ -223,18 +175,8 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   return r;
 }
 
-// Two E4M3 codes (bits 0..7 and 8..15 of `pair`) -> f16x2, exactly (every
-// E4M3 value is representable in f16).
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t pair) {
-  uint32_t r;
-  asm("{\n\t.reg .b16 t;\n\tcvt.u16.u32 t, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, t;\n\t}"
-      : "=r"(r)
-      : "r"(pair));
-  return r;
-}
-
-// Four E4M3 codes (one 32-bit word) -> two f16x2: `lo` from bytes 0-1,
-// `hi` from bytes 2-3.
+// Four E4M3 codes (one 32-bit word) -> two f16x2, exactly (every E4M3 value
+// is representable in f16): `lo` from bytes 0-1, `hi` from bytes 2-3.
 __device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
   asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
       "cvt.rn.f16x2.e4m3x2 %0, a;\n\tcvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
