@@ -1087,6 +1087,18 @@ __global__ void __launch_bounds__(NW * 32, 3)
   int cur_kvh, cur_phys, nxt_kvh, nxt_phys;
   load_window(0, cur_kvh, cur_phys);
   load_window(32, nxt_kvh, nxt_phys);
+  // bf16: the warp's first ST tiles into L2 while the previous grid drains. A
+  // prefetch consumes nothing (a line the previous grid still writes is served
+  // from L2 as written), so it may precede the dependency wait. Measured on
+  // the Llama-3-8B-shaped batch 64: 91.9 -> 89.2 us per step; the 8-bit
+  // instantiations, bound by instruction latency, gained nothing (INT8 lost 1 %).
+  if constexpr (!Q8) {
+    if (lane < ST && lane < nmine) {
+      const int pp = cur_phys >= 0 && cur_phys < a.num_blocks ? cur_phys : 0;
+      tma_prefetch_4d(&kmap, 0, pp * BS, 0, cur_kvh);
+      tma_prefetch_4d(&vmap, 0, pp * BS, 0, cur_kvh);
+    }
+  }
 
   // ---- from here on: memory the previous launch may write
   grid_dependency_wait();

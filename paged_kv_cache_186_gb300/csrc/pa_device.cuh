@@ -113,6 +113,15 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+// Bring one 4-D tile into L2 only (no shared memory, no completion).
+__device__ __forceinline__ void tma_prefetch_4d(const CUtensorMap* map, int c0, int c1, int c2,
+                                                int c3) {
+  asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+               : "memory");
+}
+
 // One 4-byte asynchronous copy global -> shared by the calling thread (both
 // addresses 4-byte aligned); it goes through the load path, not the TMA unit.
 __device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src) {
