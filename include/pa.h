@@ -173,7 +173,7 @@ pa_status pa_decode(const void* q, const pa_kv_cache* cache, const int32_t* bloc
  *            sinks ignored).
  *   sinks    >= 0: leading keys always attended (PA_ERR_SHAPE if negative).
  *   other arguments as pa_decode (same workspace size). Blocks that hold no
- *   visible key are not read. Batches above 8192 return PA_ERR_UNSUPPORTED.
+ *   visible key are not read. Batches above 16384 return PA_ERR_UNSUPPORTED.
  */
 pa_status pa_decode_window(const void* q, const pa_kv_cache* cache, const int32_t* block_tables,
                            int32_t max_blocks_per_seq, const int32_t* context_lens,
@@ -198,7 +198,7 @@ pa_status pa_decode_window(const void* q, const pa_kv_cache* cache, const int32_
  * pa_store_kv with that slot mapping followed by pa_decode. The block holding
  * position p must not be read by another sequence of the same call. A
  * physical block id out of range skips the write and sets
- * PA_DEVERR_BLOCK_RANGE. With the persistent kernel (batch <= 8192) the warp
+ * PA_DEVERR_BLOCK_RANGE. With the persistent kernel (batch <= 16384) the warp
  * that attends to a sequence's last block also writes the row; larger batches
  * use a separate store launch first.
  */
@@ -275,7 +275,7 @@ pa_status pa_get_device_error(uint32_t* code);
  * lets the copies it has in flight land (each wait bounded again) and returns,
  * so the context stays usable. This hook makes that happen on purpose without
  * faulting anything: while armed (skip_copy >= 0), decode launches of this
- * process (persistent kernel, batch <= 8192; pa_decode, pa_decode_window,
+ * process (persistent kernel, batch <= 16384; pa_decode, pa_decode_window,
  * pa_decode_append) wait at most wait_limit_ns (1 .. 2e9) per copy, and in
  * each launch the first warp of the first CTA never issues its skip_copy-th
  * block copy (counted from 0 in its own block order), so its wait for that

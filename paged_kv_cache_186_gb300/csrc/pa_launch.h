@@ -41,7 +41,7 @@ cudaError_t launch_store_new_tokens(const StoreArgs& a, const int32_t* block_tab
 // per-(slot, head) scales in E4M3 or INT8.
 constexpr int kKvBf16 = 0, kKvE4m3 = 1, kKvInt8 = 2;
 
-constexpr int kMaxPersistentBatch = 8192;
+constexpr int kMaxPersistentBatch = 16384;
 
 struct DecodeArgs {
   const void* q;              // (B, H, D) bf16

@@ -140,7 +140,8 @@ def _full_size(name):
 
 @pytest.mark.parametrize("name", ["llama3_8b_decode_b64", "long_context_decode_b8",
                                   "llama3_70b_fp8_decode_b256", "llama3_8b_short_decode_b2304",
-                                  "llama3_8b_short_decode_b9216"])
+                                  "llama3_8b_short_decode_b9216",
+                                  "llama3_8b_short_decode_b17408"])
 def test_full_size_workload_every_sequence(name):
     # the bench's launch configuration; every output row against the oracle
     got, want = _full_size(name)
@@ -209,21 +210,21 @@ def test_merge_group_boundaries(H, Hkv, kv, L):
 
 
 def test_batch_at_persistent_limit():
-    # 8192 sequences: the largest batch of the persistent kernel (its prefix
-    # sums fill 32 KB of shared memory, 2 CTAs per SM)
+    # 16384 sequences: the largest batch of the persistent kernel (its prefix
+    # sums fill 64 KB of shared memory, 1 CTA per SM)
     gen = torch.Generator().manual_seed(95)
-    lens = torch.randint(0, 40, (8192,), generator=gen).tolist()
+    lens = torch.randint(0, 40, (16384,), generator=gen).tolist()
     lens[4000] = 3000  # one segment split over many warps
-    h = W.make_decode(8192, 8, 2, 64, 16, lens, seed=96)
+    h = W.make_decode(16384, 8, 2, 64, 16, lens, seed=96)
     got, want = run_case(h, max_context_len=max(lens))
     assert torch.all(got[torch.tensor(lens) == 0].float() == 0)
-    assert_attention_close(got, want, "batch 8192")
+    assert_attention_close(got, want, "batch 16384")
 
 
 def test_batch_above_persistent_limit_uses_grid_split():
     gen = torch.Generator().manual_seed(93)
-    lens = torch.randint(1, 40, (8300,), generator=gen).tolist()
+    lens = torch.randint(1, 40, (16500,), generator=gen).tolist()
     lens[7] = 700  # one sequence long enough to need several splits
-    h = W.make_decode(8300, 8, 2, 64, 16, lens, seed=94)
+    h = W.make_decode(16500, 8, 2, 64, 16, lens, seed=94)
     got, want = run_case(h, max_context_len=max(lens))
     assert_attention_close(got, want, "large batch")

@@ -130,9 +130,9 @@ def test_append_long_sequence_split_across_warps():
 
 def test_append_batch_above_persistent_limit():
     gen = torch.Generator().manual_seed(166)
-    lens = torch.randint(1, 40, (8300,), generator=gen).tolist()
+    lens = torch.randint(1, 40, (16500,), generator=gen).tolist()
     lens[7] = 700
-    h = W.make_decode(8300, 8, 2, 64, 16, lens, seed=167)
+    h = W.make_decode(16500, 8, 2, 64, 16, lens, seed=167)
     want = oracle_store_and_decode(h)
     got = assert_same_as_separate(to_device(h), max_context_len=max(lens))
     assert_attention_close(got, want, "large batch")

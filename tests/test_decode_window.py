@@ -131,7 +131,7 @@ def test_window_rejects_negative_sinks_and_large_batches():
                             ctypes.c_void_p(g.q.data_ptr()), ctypes.c_void_p(ws.data_ptr()),
                             ws.numel(), None)
     assert rc == 2  # PA_ERR_SHAPE
-    B = 8300  # grid-split path: no window support
+    B = 16500  # grid-split path: no window support
     need = pa.decode_workspace_size(g.k_cache, B, 8, g.block_tables.shape[1], 64)
     big = torch.empty(max(need, 16), dtype=torch.uint8, device="cuda")
     rc = L.pa_decode_window(ctypes.c_void_p(g.q.data_ptr()), ctypes.byref(cache),

@@ -101,10 +101,10 @@ def test_noalloc_calls_with_changing_shapes():
 
 def test_noalloc_rejects_shapes_beyond_its_scratch():
     g = to_device(W.make_decode(2, 64, 8, 128, 32, [40, 70], seed=71, kv_dtype="fp8"))
-    # claimed shape: a batch above the persistent kernel's 8192 sequences (the
+    # claimed shape: a batch above the persistent kernel's 16384 sequences (the
     # grid-split path), whose split-K scratch grows with batch x context and
     # far exceeds the static buffer
-    B, H = 9000, 64
+    B, H = 17000, 64
     need = pa.decode_workspace_size(g.k_cache, B, H, 512, 16384, k_scale=g.k_scale,
                                     v_scale=g.v_scale)
     assert need > pa.DECODE_NOALLOC_SCRATCH_BYTES

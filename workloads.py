@@ -64,14 +64,21 @@ WORKLOADS = {
                                          lens=("lognormal", 96.0, 1.0, 8, 1536),
                                          pool_factor=1.1, scale=1.0 / math.sqrt(128),
                                          kv_dtype="bf16"),
-    # More sequences than the persistent decode's per-sequence prefix sums
-    # hold (8192): the grid-split decode. Llama-3-8B heads, short contexts
-    # (lognormal, median 64, sigma 0.5, clipped to [8, 512]).
+    # 9216 sequences, Llama-3-8B heads, short contexts (lognormal, median 64,
+    # sigma 0.5, clipped to [8, 512]): the persistent decode at 2 CTAs per SM.
     "llama3_8b_short_decode_b9216": dict(kind="decode", seed=6, batch=9216, num_heads=32,
                                          num_kv_heads=8, head_dim=128, block_size=16,
                                          lens=("lognormal", 64.0, 0.5, 8, 512),
                                          pool_factor=1.1, scale=1.0 / math.sqrt(128),
                                          kv_dtype="bf16"),
+    # More sequences than the persistent decode's per-sequence prefix sums
+    # hold (16384): the grid-split decode. Llama-3-8B heads, short contexts
+    # (lognormal, median 48, sigma 0.5, clipped to [8, 384]).
+    "llama3_8b_short_decode_b17408": dict(kind="decode", seed=8, batch=17408, num_heads=32,
+                                          num_kv_heads=8, head_dim=128, block_size=16,
+                                          lens=("lognormal", 48.0, 0.5, 8, 384),
+                                          pool_factor=1.1, scale=1.0 / math.sqrt(128),
+                                          kv_dtype="bf16"),
     # Varlen prefix-cached prefill: 8 sequences, 32/8 heads, D=128, bs=16,
     # cached_len uniform in [0, 2048], q_len uniform in [128, 1024].
     "varlen_prefill_b8": dict(kind="prefill", seed=4, batch=8, num_heads=32, num_kv_heads=8,
