@@ -147,9 +147,12 @@ size_t pa_decode_workspace_size(const pa_kv_cache* cache, int32_t batch, int32_t
  *   out             (batch, num_heads, head_dim) bf16.
  *   workspace       device scratch of at least pa_decode_workspace_size()
  *                   bytes (may be NULL when that is 0). Contents on entry are
- *                   ignored; calls sharing one workspace must not overlap.
- *                   The split-K arrival counters in it carry a per-call tag
- *                   and each is cleared by its last arrival, so a CUDA graph
+ *                   ignored, up to a 2^-32 chance per stale 64-bit word of
+ *                   carrying the call's tag; calls sharing one workspace must
+ *                   not overlap.
+ *                   The split-K arrival counters in it carry a per-call
+ *                   32-bit tag (unrelated from call to call) and each is
+ *                   cleared by its last arrival, so a CUDA graph
  *                   that captured the call can be replayed back to back on
  *                   the same workspace (its tag is frozen at capture). After
  *                   a launch that reported PA_DEVERR_WAIT_TIMEOUT, counters

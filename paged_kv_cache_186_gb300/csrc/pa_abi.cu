@@ -176,13 +176,22 @@ pa_status cached_cache_map(CUtensorMap* out, void* base, const pa_kv_cache* c, i
 std::atomic<int> g_debug_skip_copy{-1};
 std::atomic<unsigned long long> g_debug_wait_limit_ns{0};
 
-// Tag of one decode call in the workspace's arrival counters: increasing,
-// never 0 (a zeroed counter never matches the current call).
+// Tag of one decode call in the workspace's arrival counters: a call counter
+// passed through a 64-bit finalising mix (the one of SplitMix64, a bijection
+// of 64-bit words), upper half kept, never 0 (a zeroed counter never matches
+// the current call). Consecutive calls thus get unrelated tags, and a word of
+// arbitrary earlier contents carries the current call's tag with probability
+// 2^-32, not "whenever it holds a small integer".
 uint32_t next_epoch() {
-  static std::atomic<uint32_t> counter{0};
-  uint32_t e = counter.fetch_add(1) + 1;
-  if (e == 0) e = counter.fetch_add(1) + 1;
-  return e;
+  static std::atomic<uint64_t> counter{0};
+  while (true) {
+    uint64_t z = counter.fetch_add(1) + 0x9e3779b97f4a7c15ull;
+    z = (z ^ (z >> 30)) * 0xbf58476d1ce4e5b9ull;
+    z = (z ^ (z >> 27)) * 0x94d049bb133111ebull;
+    z ^= z >> 31;
+    const uint32_t e = static_cast<uint32_t>(z >> 32);
+    if (e != 0) return e;
+  }
 }
 
 int decode_len_cap(const pa_kv_cache* c, int32_t max_blocks_per_seq, int32_t max_context_len) {
