@@ -101,6 +101,31 @@ def test_repeat_calls_are_deterministic():
     assert torch.equal(a.view(torch.int16), b.view(torch.int16))
 
 
+def test_workspace_contents_on_entry_are_ignored():
+    # zeros, all-ones bytes, random bytes and a workspace an earlier call left
+    # behind: the same output, equal to the oracle's (segments split across warps)
+    lens = [3000, 17, 4096, 1, 1500, 2200, 700, 64]
+    h = W.make_decode(len(lens), 32, 8, 128, 16, lens, seed=73)
+    want = oracle_store_and_decode(h)
+    g = to_device(h)
+    n = pa.decode_workspace_size(g.k_cache, len(lens), 32, g.block_tables.shape[1])
+    assert n > 0
+    first = gpu_store_decode(g).clone()
+    assert_attention_close(first, want, "first call")
+    gen = torch.Generator().manual_seed(74)
+    left_behind = torch.empty(n, dtype=torch.uint8, device="cuda")
+    pa.decode(g.q, g.k_cache, g.v_cache, g.block_tables, g.context_lens, g.scale,
+              workspace=left_behind)
+    fills = [torch.zeros(n, dtype=torch.uint8), torch.full((n,), 255, dtype=torch.uint8),
+             torch.randint(0, 256, (n,), generator=gen, dtype=torch.uint8)]
+    for ws in [f.cuda() for f in fills] + [left_behind]:
+        got = pa.decode(g.q, g.k_cache, g.v_cache, g.block_tables, g.context_lens, g.scale,
+                        workspace=ws)
+        torch.cuda.synchronize()
+        assert pa.get_device_error() == 0
+        assert torch.equal(got.view(torch.int16), first.view(torch.int16))
+
+
 def test_workspace_too_small_is_rejected():
     h = to_device(W.make_decode(2, 32, 8, 128, 16, [4000, 4000], seed=66))
     need = pa.decode_workspace_size(h.k_cache, 2, 32, h.block_tables.shape[1])
