@@ -16,6 +16,35 @@ namespace {
 
 constexpr int kStoreWarps = 4;
 
+// A token's K and V rows (n16 16-byte chunks each) copied by one warp: every
+// lane first issues the loads of all its chunks (up to kChunksPerLane each of
+// K and V per round), then the stores, so a row costs one load round trip
+// instead of one per 512 bytes (the loads of a round could not pass the
+// stores of the previous one: the cache may alias the inputs).
+constexpr int kChunksPerLane = 8;
+__device__ __forceinline__ void copy_rows(const uint4* ks, const uint4* vs, uint4* kd, uint4* vd,
+                                          int n16, int lane) {
+  for (int base = 0; base < n16; base += 32 * kChunksPerLane) {
+    uint4 kb[kChunksPerLane], vb[kChunksPerLane];
+#pragma unroll
+    for (int j = 0; j < kChunksPerLane; ++j) {
+      const int i = base + lane + 32 * j;
+      if (i < n16) {
+        kb[j] = __ldg(ks + i);
+        vb[j] = __ldg(vs + i);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < kChunksPerLane; ++j) {
+      const int i = base + lane + 32 * j;
+      if (i < n16) {
+        kd[i] = kb[j];
+        vd[i] = vb[j];
+      }
+    }
+  }
+}
+
 __global__ void __launch_bounds__(kStoreWarps * 32) store_kv_kernel(const StoreArgs a) {
   grid_launch_dependents();  // a following decode/prefill may start its prologue
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -34,12 +63,7 @@ __global__ void __launch_bounds__(kStoreWarps * 32) store_kv_kernel(const StoreA
                                                    static_cast<long long>(t) * a.row_bytes);
   uint4* kd = reinterpret_cast<uint4*>(static_cast<char*>(a.k_cache) + slot * a.row_bytes);
   uint4* vd = reinterpret_cast<uint4*>(static_cast<char*>(a.v_cache) + slot * a.row_bytes);
-  for (int i = lane; i < n16; i += 32) {
-    const uint4 kv = __ldg(ks + i);
-    const uint4 vv = __ldg(vs + i);
-    kd[i] = kv;
-    vd[i] = vv;
-  }
+  copy_rows(ks, vs, kd, vd, n16, lane);
   if (a.k_scale != nullptr) {
     // scales: new (T, Hkv) -> cache (num_blocks, Hkv, block_size)
     const long long blk = slot / a.block_size, off = slot % a.block_size;
@@ -77,12 +101,7 @@ __global__ void __launch_bounds__(kStoreWarps * 32)
                                                    static_cast<long long>(t) * a.row_bytes);
   uint4* kd = reinterpret_cast<uint4*>(static_cast<char*>(a.k_cache) + slot * a.row_bytes);
   uint4* vd = reinterpret_cast<uint4*>(static_cast<char*>(a.v_cache) + slot * a.row_bytes);
-  for (int i = lane; i < n16; i += 32) {
-    const uint4 kv = __ldg(ks + i);
-    const uint4 vv = __ldg(vs + i);
-    kd[i] = kv;
-    vd[i] = vv;
-  }
+  copy_rows(ks, vs, kd, vd, n16, lane);
   if (a.k_scale != nullptr) {
     const long long off = slot % a.block_size;
     for (int h = lane; h < a.num_kv_heads; h += 32) {
