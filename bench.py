@@ -488,13 +488,16 @@ class DecodeBench:
         self.out = torch.empty((self.B, w["num_heads"], w["head_dim"]), dtype=torch.bfloat16,
                                device=dev)
         self.stream = torch.cuda.current_stream()
-        # the fused append has no window variant
-        self.fused = step_kind == "append" and window <= 0
+        # the fused append (with or without a window): one persistent launch
+        self.fused = step_kind == "append"
         # store_kv + decode (or the fused append: one persistent launch); the
-        # grid-split path (batches above 2048) adds a merge
-        self.launches_per_step = (1 if self.fused else 2) if self.B <= 2048 else 3
+        # grid-split path (batches above 16384) stores first and adds a merge
+        self.launches_per_step = (1 if self.fused else 2) if self.B <= 16384 else 3
 
     def describe_step(self):
+        if self.fused and self.window > 0:
+            return (f"decode_window_append (store of the new tokens fused into the windowed "
+                    f"decode; window {self.window}, sinks {self.sinks})")
         if self.fused:
             return "decode_append (store of the new tokens fused into decode)"
         if self.window > 0:
@@ -508,11 +511,12 @@ class DecodeBench:
         if self.fused:
             if ev is not None:
                 ev[0].record(self.stream)
-            pa.decode_append(x["q"], x["k_new"], x["v_new"], p.k_cache, p.v_cache,
-                             x["block_tables"], x["context_lens"], p.scale,
-                             max_context_len=self.max_len, out=out, workspace=self.workspace,
-                             k_scale_new=x.get("k_scale_new"), v_scale_new=x.get("v_scale_new"),
-                             k_scale=p.k_scale, v_scale=p.v_scale)
+            pa.decode_window_append(x["q"], x["k_new"], x["v_new"], p.k_cache, p.v_cache,
+                                    x["block_tables"], x["context_lens"], p.scale, self.window,
+                                    self.sinks, max_context_len=self.max_len, out=out,
+                                    workspace=self.workspace, k_scale_new=x.get("k_scale_new"),
+                                    v_scale_new=x.get("v_scale_new"), k_scale=p.k_scale,
+                                    v_scale=p.v_scale)
             if ev is not None:
                 ev[1].record(self.stream)
             return

@@ -214,6 +214,24 @@ pa_status pa_decode_append(const void* q, const void* k_new, const void* v_new,
                            void* stream);
 
 /*
+ * pa_decode_window_append - pa_decode_append with the sliding window and
+ * attention sinks of pa_decode_window: the new row is written as by
+ * pa_decode_append, then each query attends to the keys pa_decode_window
+ * selects (the new token, at position context_len - 1, is always among them).
+ * Result and cache contents are those of pa_store_kv followed by
+ * pa_decode_window; window 0 is pa_decode_append. Same arguments as
+ * pa_decode_append plus window and sinks (as pa_decode_window); batches above
+ * 16384 return PA_ERR_UNSUPPORTED, as for pa_decode_window.
+ */
+pa_status pa_decode_window_append(const void* q, const void* k_new, const void* v_new,
+                                  const float* k_scale_new, const float* v_scale_new,
+                                  const pa_kv_cache* cache, const int32_t* block_tables,
+                                  int32_t max_blocks_per_seq, const int32_t* context_lens,
+                                  int32_t max_context_len, int32_t batch, int32_t num_heads,
+                                  float scale, int32_t window, int32_t sinks, void* out,
+                                  void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * pa_prefill_varlen - prefill attention of packed new tokens over their
  * sequences' paged K/V (cached prefix + the new tokens, which must already be
  * stored with pa_store_kv), with the bottom-right-aligned causal mask: query

@@ -37,7 +37,8 @@ DECODE_NOALLOC_SCRATCH_BYTES = 32 << 20
 
 # Every symbol include/pa.h declares.
 EXPORTED = ("pa_abi_version", "pa_status_string", "pa_store_kv", "pa_decode_workspace_size",
-            "pa_decode", "pa_decode_window", "pa_decode_append", "pa_prefill_varlen",
+            "pa_decode", "pa_decode_window", "pa_decode_append", "pa_decode_window_append",
+            "pa_prefill_varlen",
             "pa_decode_noalloc", "pa_get_device_error", "pa_debug_inject_wait_timeout")
 
 
@@ -86,6 +87,10 @@ def lib() -> ctypes.CDLL:
     L.pa_decode_append.restype = ctypes.c_int
     L.pa_decode_append.argtypes = [P, P, P, P, P, ctypes.POINTER(KVCache), P, i32, P, i32, i32,
                                    i32, ctypes.c_float, P, P, ctypes.c_size_t, P]
+    L.pa_decode_window_append.restype = ctypes.c_int
+    L.pa_decode_window_append.argtypes = [P, P, P, P, P, ctypes.POINTER(KVCache), P, i32, P, i32,
+                                          i32, i32, ctypes.c_float, i32, i32, P, P,
+                                          ctypes.c_size_t, P]
     L.pa_prefill_varlen.restype = ctypes.c_int
     L.pa_prefill_varlen.argtypes = [P, ctypes.POINTER(KVCache), P, i32, P, P, i32, i32, i32, i32,
                                     ctypes.c_float, P, P]
@@ -219,6 +224,20 @@ def decode_append(q, k_new, v_new, k_cache, v_cache, block_tables, context_lens,
     """pa_decode_append: write each sequence's new K/V row (k_new/v_new
     (B, Hkv, D), cache dtype) at position context_len-1 through the block
     table, in place, and return decode attention over context_len keys."""
+    return decode_window_append(q, k_new, v_new, k_cache, v_cache, block_tables, context_lens,
+                                scale, 0, 0, max_context_len=max_context_len, out=out,
+                                workspace=workspace, k_scale_new=k_scale_new,
+                                v_scale_new=v_scale_new, k_scale=k_scale, v_scale=v_scale)
+
+
+def decode_window_append(q, k_new, v_new, k_cache, v_cache, block_tables, context_lens,
+                         scale: float, window: int, sinks: int = 0, *, max_context_len: int = 0,
+                         out=None, workspace=None, k_scale_new=None, v_scale_new=None,
+                         k_scale=None, v_scale=None) -> torch.Tensor:
+    """pa_decode_window_append (window 0: pa_decode_append): write each
+    sequence's new K/V row at position context_len-1 through the block table,
+    in place, and return decode attention over the last `window` keys and the
+    first `sinks` keys (window <= 0: all context_len keys)."""
     cache = make_cache(k_cache, v_cache, k_scale, v_scale)
     B, H, D = q.shape
     bt = block_tables.contiguous()
@@ -232,11 +251,19 @@ def decode_append(q, k_new, v_new, k_cache, v_cache, block_tables, context_lens,
         if need:
             workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    _check(lib().pa_decode_append(_ptr(q.contiguous()), _ptr(k_new), _ptr(v_new),
-                                  _ptr(k_scale_new), _ptr(v_scale_new), ctypes.byref(cache),
-                                  _ptr(bt), bt.shape[1], _ptr(cl), int(max_context_len), B, H,
-                                  float(scale), _ptr(out), _ptr(workspace), ws_bytes, _stream()),
-           "pa_decode_append")
+    if int(window) > 0:
+        rc = lib().pa_decode_window_append(
+            _ptr(q.contiguous()), _ptr(k_new), _ptr(v_new), _ptr(k_scale_new), _ptr(v_scale_new),
+            ctypes.byref(cache), _ptr(bt), bt.shape[1], _ptr(cl), int(max_context_len), B, H,
+            float(scale), int(window), int(sinks), _ptr(out), _ptr(workspace), ws_bytes,
+            _stream())
+        _check(rc, "pa_decode_window_append")
+    else:
+        rc = lib().pa_decode_append(
+            _ptr(q.contiguous()), _ptr(k_new), _ptr(v_new), _ptr(k_scale_new), _ptr(v_scale_new),
+            ctypes.byref(cache), _ptr(bt), bt.shape[1], _ptr(cl), int(max_context_len), B, H,
+            float(scale), _ptr(out), _ptr(workspace), ws_bytes, _stream())
+        _check(rc, "pa_decode_append")
     return out
 
 

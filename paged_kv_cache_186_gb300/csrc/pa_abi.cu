@@ -408,6 +408,18 @@ pa_status pa_decode_append(const void* q, const void* k_new, const void* v_new,
                            int32_t max_context_len, int32_t batch, int32_t num_heads,
                            float scale, void* out, void* workspace, size_t workspace_bytes,
                            void* stream) {
+  return pa_decode_window_append(q, k_new, v_new, k_scale_new, v_scale_new, cache, block_tables,
+                                 max_blocks_per_seq, context_lens, max_context_len, batch,
+                                 num_heads, scale, 0, 0, out, workspace, workspace_bytes, stream);
+}
+
+pa_status pa_decode_window_append(const void* q, const void* k_new, const void* v_new,
+                                  const float* k_scale_new, const float* v_scale_new,
+                                  const pa_kv_cache* cache, const int32_t* block_tables,
+                                  int32_t max_blocks_per_seq, const int32_t* context_lens,
+                                  int32_t max_context_len, int32_t batch, int32_t num_heads,
+                                  float scale, int32_t window, int32_t sinks, void* out,
+                                  void* workspace, size_t workspace_bytes, void* stream) {
   pa_status st = check_cache(cache);
   if (st != PA_OK) return st;
   if (batch > 0 && (k_new == nullptr || v_new == nullptr)) return PA_ERR_NULL;
@@ -416,7 +428,7 @@ pa_status pa_decode_append(const void* q, const void* k_new, const void* v_new,
   if (batch > 0 && (!aligned16(k_new) || !aligned16(v_new))) return PA_ERR_ALIGN;
   return decode_common(q, cache, block_tables, max_blocks_per_seq, context_lens, max_context_len,
                        batch, num_heads, scale, out, workspace, workspace_bytes, stream, k_new,
-                       v_new, k_scale_new, v_scale_new, 0, 0);
+                       v_new, k_scale_new, v_scale_new, window, sinks);
 }
 
 pa_status pa_prefill_varlen(const void* q, const pa_kv_cache* cache, const int32_t* block_tables,

@@ -140,3 +140,40 @@ def test_window_rejects_negative_sinks_and_large_batches():
                             ctypes.c_void_p(g.q.data_ptr()), ctypes.c_void_p(big.data_ptr()),
                             big.numel(), None)
     assert rc == 4  # PA_ERR_UNSUPPORTED, nothing launched
+
+
+APPEND_CASES = [
+    # (H, Hkv, bs, kv, lens, window, sinks)
+    (32, 8, 16, "bf16", [1, 5, 300, 1100, 5000, 2049, 0, 4100], 1024, 4),
+    (32, 8, 16, "bf16", [40, 41, 300, 17], 20, 10),               # hole inside one block
+    (8, 1, 16, "bf16", [9, 300, 1025], 1, 0),                     # newest key only
+    (64, 8, 32, "fp8", [1, 31, 33, 1000, 5000], 256, 4),
+    (64, 8, 32, "int8", [2, 64, 65, 3000], 100, 3),
+]
+
+
+@pytest.mark.parametrize("case", APPEND_CASES,
+                         ids=lambda c: f"{c[3]}_w{c[5]}s{c[6]}_H{c[0]}kv{c[1]}bs{c[2]}")
+def test_window_append_equals_store_then_window(case):
+    # pa_decode_window_append: the new rows written by the decode's own warps,
+    # then the window; bit-identical to pa_store_kv + pa_decode_window (outputs
+    # and cache bytes) and within tolerance of the oracle
+    H, Hkv, bs, kv, lens, window, sinks = case
+    h = W.make_decode(len(lens), H, Hkv, 128, bs, lens, seed=211 + H + bs + window, kv_dtype=kv)
+    want = oracle_window(h, window, sinks)
+    fused, sep = to_device(h), to_device(h)
+    got = pa.decode_window_append(fused.q, fused.k_new, fused.v_new, fused.k_cache, fused.v_cache,
+                                  fused.block_tables, fused.context_lens, fused.scale, window,
+                                  sinks, k_scale_new=fused.k_scale_new,
+                                  v_scale_new=fused.v_scale_new, k_scale=fused.k_scale,
+                                  v_scale=fused.v_scale)
+    torch.cuda.synchronize()
+    assert pa.get_device_error() == 0
+    ref = gpu_window(sep, window, sinks)
+    assert torch.equal(got.view(torch.int16), ref.view(torch.int16))
+    assert torch.equal(fused.k_cache.view(torch.uint8), sep.k_cache.view(torch.uint8))
+    assert torch.equal(fused.v_cache.view(torch.uint8), sep.v_cache.view(torch.uint8))
+    if kv != "bf16":
+        assert torch.equal(fused.k_scale, sep.k_scale) and torch.equal(fused.v_scale, sep.v_scale)
+    assert_attention_close(got, want, f"window append {case}")
+    assert torch.all(got[torch.tensor(lens) == 0].float() == 0)
