@@ -625,22 +625,32 @@ __device__ __forceinline__ void write_warp_result(const DecodeArgs& a, int b, in
   }
 }
 
-// Warps that take part: one per kBlocksPerWarp blocks of work (fewer pieces
-// and merges; measured best from batch 4 to 64 at ~2k tokens), but at least
-// one per kMinBlocksPerWarp blocks (one per block for short segments) up to
-// one warp per CTA, so that small problems keep
-// some parallelism, and at most kMaxPartsPerSegment per (sequence, kv head)
-// segment. Segments of more than kGroupedAbove parts merge in two levels, so
-// no warp merges more than max(kGroupedAbove, kMergeGroup + the number of
-// groups) partials. (A warp whose share of the work units holds no block
-// has nothing to do.)
-constexpr int kBlocksPerWarp = 16;
+// Warps that take part: about one per 10 blocks of work (N * 51 / 512, a
+// multiply and a shift: with a 64-bit divide by 12 here the 8-bit batch-256
+// steps, whose warp count it does not change, ran 0.4 % slower), but at
+// least one per kMinBlocksPerWarp blocks
+// (one per block for short segments) up to one warp per CTA, so that small
+// problems keep some parallelism, and at most kMaxPartsPerSegment per
+// (sequence, kv head) segment. Problems of more than ~10 blocks per warp of
+// the grid use every warp either way. Measured by graph replay on one GB300
+// (bf16, 32/8 heads, 16-token blocks), one warp per 16 blocks -> per 10:
+// batch 8 x 2048 tokens 21.7 -> 18.2 us, 32 x 1024 27.9 -> 25.0, 64 x 512
+// 27.8 -> 24.4, 2 x 12000 27.3 -> 25.7, 8 x 4096 30.0 -> 29.6, 16 x 2048
+// 26.4 -> 26.5. One per 12 or 14 blocks was slower overall; one per 8 or 9
+// was faster on some of these and slower on the windowed steps.
+// Segments of more than kGroupedAbove parts merge in two levels, so no warp
+// merges more than max(kGroupedAbove, kMergeGroup + the number of groups)
+// partials. (A warp whose share of the work units holds no block has nothing
+// to do.)
+constexpr long long kWarpsPerBlockNum = 51;  // warps = N * 51 >> 9, about N / 10
+constexpr int kWarpsPerBlockShift = 9;
 constexpr int kMinBlocksPerWarp = 4;
 constexpr int kMaxPartsPerSegment = 1024;
 __device__ __forceinline__ long long active_warps(long long N, long long ctas, long long warps,
                                                   long long segments, bool one_block_floor) {
   // (no division by a run-time value: a 64-bit divide here costs registers)
-  long long w = max(N / kBlocksPerWarp, min(one_block_floor ? N : N / kMinBlocksPerWarp, ctas));
+  long long w = max((N * kWarpsPerBlockNum) >> kWarpsPerBlockShift,
+                    min(one_block_floor ? N : N / kMinBlocksPerWarp, ctas));
   w = min(w, segments * kMaxPartsPerSegment);
   return max(1LL, min(warps, w));
 }
