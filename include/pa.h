@@ -250,7 +250,9 @@ pa_status pa_decode_window_append(const void* q, const void* k_new, const void* 
  * as 0 and keys are clamped to kv_len. Supported: bf16 cache, head_dim 128,
  * block_size 16 or 32, num_heads/num_kv_heads in {1, 2, 4, 8, 16}.
  * Arithmetic: bf16 operands on the tensor cores, fp32 scores and
- * accumulation, probabilities rounded to bf16 for P.V, bf16 output.
+ * accumulation, probabilities rounded to bf16 for P.V (as two bf16 terms,
+ * bf16(p) + bf16(p - bf16(p)), on the first 128 keys of the query tiles that
+ * hold rows seeing fewer than 128 keys), bf16 output.
  */
 pa_status pa_prefill_varlen(const void* q, const pa_kv_cache* cache, const int32_t* block_tables,
                             int32_t max_blocks_per_seq, const int32_t* cu_seqlens_q,

@@ -32,6 +32,17 @@
 //     (the running max is only raised, and O rescaled, when it grows by more
 //     than 2^8, which keeps P <= 256 and leaves O/l unchanged), write P as
 //     bf16 into the S columns, and at the end normalise O and store bf16 rows.
+//   * P precision: one bf16 rounding of P is 2^-9 relative per weight. Over
+//     many keys the errors average out (worst |error| ~4e-3 at 128 keys in
+//     20k random rows, falling with more keys), but a row that sees only a
+//     few keys keeps its weights' rounding whole: 2-4 keys reached 1.0-1.1e-2
+//     before the output's own bf16 rounding. So on key tile 0 of a query tile
+//     whose first row sees fewer than 128 keys (all of such a row's keys lie
+//     in tile 0), P goes in as two bf16 terms, bf16(p) in columns 0..63 and
+//     bf16(p - bf16(p)) in columns 64..127 of S, and that P.V takes 16 MMAs
+//     instead of 8. Tiles of rows with longer prefixes are unchanged; the
+//     code's presence costs ~3 % there (measured 124.2 -> 128.4 us on the
+//     8-sequence benchmark, whose prefixes are all >= 250 tokens).
 //   * TMEM: 512 columns (S0, S1, O0, O1, 128 each); shared memory: Q0, Q1,
 //     two K and two V stages (192 KB).
 #include <algorithm>
@@ -57,10 +68,11 @@ static_assert(kSmem <= 227 * 1024, "shared memory over the per-CTA limit");
 static_assert(32 % (kBN / 16) == 0 && 32 % (kBN / 32) == 0, "tiles must not straddle a block-id window");
 constexpr int kThreads = 384;          // 2 x 4 softmax warps, K producer, MMA, V producer, idle
 // Register split (setmaxnreg): launched at 65536/384 -> 168 per thread; the
-// producer/MMA warpgroup drops to 72 so the two softmax warpgroups can hold a
-// whole 128-key score row: 2*128*216 + 128*72 = 384*168.
-constexpr int kSoftmaxRegs = 216;
-constexpr int kControlRegs = 72;
+// producer/MMA warpgroup drops to 88 so the two softmax warpgroups can hold a
+// whole 128-key score row: 2*128*208 + 128*88 = 384*168. (216/72 left the
+// MMA warp no room for the two-term P.V below: it spilled or ran slower.)
+constexpr int kSoftmaxRegs = 208;
+constexpr int kControlRegs = 88;
 static_assert(2 * 128 * kSoftmaxRegs + 128 * kControlRegs <= kThreads * 168,
               "register split exceeds the launch allocation");
 constexpr uint32_t kTmemCols = 512;
@@ -140,6 +152,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   Tq[0] = (min(cached + min(t00 + TPT, q_len), kv_len) + kBN - 1) / kBN;
   Tq[1] = has1 ? (min(cached + min(t00 + 2 * TPT, q_len), kv_len) + kBN - 1) / kBN : 0;
   const int T = max(Tq[0], Tq[1]);
+  // P.V takes P as two bf16 terms on key tile 0 of a query tile whose first
+  // row sees fewer than kBN keys (every key of such a row lies in tile 0)
+  auto two_term = [&](int i) { return cached + t00 + i * TPT < kBN; };
   __nv_bfloat16* const out = static_cast<__nv_bfloat16*>(a.out);
   const int H = a.num_heads;
 
@@ -265,12 +280,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     auto issue_pv = [&](int i, int n) {  // O_i += P_i V(n)
       const int vs = n % kVStages;
+      const int terms = n == 0 && two_term(i) ? 2 : 1;
       tc::fence_after_sync();
       if (lane == 0) {
+#pragma unroll 1
+        for (int t = 0; t < terms; ++t) {  // P = hi (columns 0..63) + lo (64..127)
 #pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk)
-          tc::mma_ts(tO(i), tS(i) + kk * 8, tc::smem_desc_sw128(v_s(vs) + kk * 16 * 128, kSub, 1024),
-                     kIdescPV, (n > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < kBN / 16; ++kk)
+            tc::mma_ts(tO(i), tS(i) + 64 * t + kk * 8,
+                       tc::smem_desc_sw128(v_s(vs) + kk * 16 * 128, kSub, 1024), kIdescPV,
+                       (n > 0 || kk > 0 || t > 0) ? 1u : 0u);
+        }
         tc::commit(bar(BAR_O + i));
       }
       __syncwarp();
@@ -413,6 +433,26 @@ __global__ void __launch_bounds__(kThreads, 1)
           w[j] = pack_bf16x2(p0, p1);
         }
         tc::tmem_st32(tS(ti) + trow + 32 * h, w);
+      }
+      if (n == 0 && two_term(ti)) {
+        // second term of P, p - bf16(p) as bf16, into columns 64..127: P is
+        // computed again from the scores (the same operations, the same values)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t w[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int c = 2 * h + (j >> 4), e = 2 * (j & 15);
+            const uint64_t xa = tc::fma_f32x2(
+                tc::f32x2(__uint_as_float(u[c][e]), __uint_as_float(u[c][e + 1])), sl2x2, nmx2);
+            float x0, x1;
+            tc::f32x2_split(xa, x0, x1);
+            const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
+            const uint32_t hi = pack_bf16x2(p0, p1);
+            w[j] = pack_bf16x2(p0 - __uint_as_float(hi << 16), p1 - __uint_as_float(hi & 0xffff0000u));
+          }
+          tc::tmem_st32(tS(ti) + trow + 64 + 32 * h, w);
+        }
       }
       {
         float la, lb;
