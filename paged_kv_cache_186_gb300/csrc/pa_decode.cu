@@ -664,6 +664,9 @@ __device__ __forceinline__ long long active_warps(long long N, long long ctas, l
 // ranges then straddle segments unevenly); longer segments unchanged.
 constexpr int kShortSegmentBlocks = 8;
 
+// Tiles each warp prefetches into L2 before the dependency wait (bf16).
+constexpr int kPrefetchTiles = 4;
+
 // Pieces of a segment that straddles warps: segment (b, kvh) over global
 // blocks [s0, s1) is split among warps w0 .. w1 (all with non-empty ranges);
 // warp w0 left its piece in slot 2*w0+1, every later one in slot 2*w.
@@ -1097,13 +1100,17 @@ __global__ void __launch_bounds__(NW * 32, 3)
   int cur_kvh, cur_phys, nxt_kvh, nxt_phys;
   load_window(0, cur_kvh, cur_phys);
   load_window(32, nxt_kvh, nxt_phys);
-  // bf16: the warp's first ST tiles into L2 while the previous grid drains. A
-  // prefetch consumes nothing (a line the previous grid still writes is served
-  // from L2 as written), so it may precede the dependency wait. Measured on
-  // the Llama-3-8B-shaped batch 64: 91.9 -> 89.2 us per step; the 8-bit
-  // instantiations, bound by instruction latency, gained nothing (INT8 lost 1 %).
+  // bf16: the warp's first kPrefetchTiles tiles into L2 while the previous
+  // grid drains. A prefetch consumes nothing (a line the previous grid still
+  // writes is served from L2 as written), so it may precede the dependency
+  // wait. Measured on the Llama-3-8B-shaped batch 64 (same box each line): no
+  // prefetch 92.0 us per step, the first 2 tiles 89.4, 4 tiles 88.0; on
+  // another box 3 / 4 / 5 / 6 tiles 85.3 / 84.6 / 85.5 / 87.1, 8 tiles worse
+  // again (the prefetches then compete with the previous grid's tail); the
+  // windowed steps gain 0.4-1 us more. The 8-bit instantiations, bound by
+  // instruction latency, gain nothing (4 tiles: E4M3 1 % slower).
   if constexpr (!Q8) {
-    if (lane < ST && lane < nmine) {
+    if (lane < kPrefetchTiles && lane < nmine) {
       const int pp = cur_phys >= 0 && cur_phys < a.num_blocks ? cur_phys : 0;
       tma_prefetch_4d(&kmap, 0, pp * BS, 0, cur_kvh);
       tma_prefetch_4d(&vmap, 0, pp * BS, 0, cur_kvh);
